@@ -1,0 +1,259 @@
+"""Pins for the fp64 oracle against things other than itself.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign, a wrong index or stride, a transposed operand, a missing max
+subtraction, a wrong log base, a broken 16-bit decode) fails at least one:
+
+* hand-worked examples (tests/golden/hand_worked.json, derivations inside);
+* brute force with math.fsum on tiny asymmetric shapes (b, sq, sk, h, d all
+  different), written from the definition without the max subtraction;
+* a library special case: torch's CPU float64 scaled_dot_product_attention
+  and logsumexp;
+* closed forms and invariants: equal V rows, sk = 1, Q = 0, equal K rows,
+  LSE bounds, joint permutation of K and V, V = identity (O = P, rows sum to
+  1), scale = 0;
+* the split-KV reduce: any split of the keys, empty splits included,
+  combines back to the unsplit result;
+* every fp16 and bf16 bit pattern decodes like numpy / torch do.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _rand(shape, seed):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape)
+
+
+# ---------------------------------------------------------------- golden
+def _load_golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _load_golden()["attention"], ids=lambda c: c["name"])
+def test_hand_worked_attention(oracle_mod, case):
+    q = np.array(case["q"], dtype=np.float64)
+    k = np.array(case["k"], dtype=np.float64)
+    v = np.array(case["v"], dtype=np.float64)
+    assert q.shape == (case["b"], case["sq"], case["h"], case["d"])
+    o, lse = oracle_mod.attention(q, k, v, case["scale"])
+    np.testing.assert_allclose(o, np.array(case["o"]), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(lse, np.array(case["lse"]), rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("case", _load_golden()["combine"], ids=lambda c: c["name"])
+def test_hand_worked_combine(oracle_mod, case):
+    lp = np.array([[float(x) for x in row] for row in case["lse_parts"]], dtype=np.float64)
+    op = np.array(case["o_parts"], dtype=np.float64)
+    o, lse = oracle_mod.combine(op, lp)
+    np.testing.assert_allclose(o, np.array(case["o"]), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(lse, np.array(case["lse"]), rtol=0, atol=1e-11)
+
+
+# ---------------------------------------------------------------- brute force
+def _brute(q, k, v, scale):
+    """Straight from the definition with exact sums; no max subtraction
+    (inputs are small, so exp cannot overflow)."""
+    b, sq, h, d = q.shape
+    sk = k.shape[1]
+    o = np.zeros((b, sq, h, d))
+    lse = np.zeros((b, h, sq))
+    for bb in range(b):
+        for hh in range(h):
+            for i in range(sq):
+                s = [scale * math.fsum(q[bb, i, hh, t] * k[bb, j, hh, t] for t in range(d))
+                     for j in range(sk)]
+                e = [math.exp(x) for x in s]
+                z = math.fsum(e)
+                for t in range(d):
+                    o[bb, i, hh, t] = math.fsum(e[j] / z * v[bb, j, hh, t] for j in range(sk))
+                lse[bb, hh, i] = math.log(z)
+    return o, lse
+
+
+@pytest.mark.parametrize("shape,scale", [((2, 3, 5, 3, 4), 0.37), ((1, 4, 1, 2, 3), -1.3),
+                                         ((3, 1, 7, 2, 5), 1.0), ((2, 6, 4, 1, 2), 0.0)])
+def test_brute_force(oracle_mod, shape, scale):
+    b, sq, sk, h, d = shape
+    q = _rand((b, sq, h, d), 1)
+    k = _rand((b, sk, h, d), 2)
+    v = _rand((b, sk, h, d), 3)
+    o, lse = oracle_mod.attention(q, k, v, scale)
+    ob, lb = _brute(q, k, v, scale)
+    np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def test_torch_sdpa_special_case(oracle_mod):
+    b, sq, sk, h, d = 2, 9, 13, 3, 8
+    scale = 0.29
+    q = _rand((b, sq, h, d), 4)
+    k = _rand((b, sk, h, d), 5)
+    v = _rand((b, sk, h, d), 6)
+    o, lse = oracle_mod.attention(q, k, v, scale)
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (q, k, v))  # (b, h, s, d)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+    ref_lse = torch.logsumexp(scale * tq @ tk.transpose(-1, -2), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- invariants
+def test_equal_v_rows_give_that_row(oracle_mod):
+    b, sq, sk, h, d = 2, 5, 11, 2, 6
+    q, k = _rand((b, sq, h, d), 7) * 3, _rand((b, sk, h, d), 8) * 3
+    c = _rand((b, 1, h, d), 9)
+    v = np.broadcast_to(c, (b, sk, h, d)).copy()
+    o, _ = oracle_mod.attention(q, k, v, 0.7)
+    np.testing.assert_allclose(o, np.broadcast_to(c, (b, sq, h, d)), rtol=0, atol=1e-13)
+
+
+def test_single_key(oracle_mod):
+    b, sq, h, d = 2, 4, 3, 5
+    q, k, v = _rand((b, sq, h, d), 10), _rand((b, 1, h, d), 11), _rand((b, 1, h, d), 12)
+    o, lse = oracle_mod.attention(q, k, v, 0.45)
+    np.testing.assert_allclose(o, np.broadcast_to(v, (b, sq, h, d)), rtol=0, atol=1e-14)
+    expect = 0.45 * np.einsum("bihd,bhd->bhi", q, k[:, 0])
+    np.testing.assert_allclose(lse, expect, rtol=0, atol=1e-13)
+
+
+def test_zero_query_is_uniform(oracle_mod):
+    b, sq, sk, h, d = 1, 3, 10, 2, 4
+    q = np.zeros((b, sq, h, d))
+    k, v = _rand((b, sk, h, d), 13), _rand((b, sk, h, d), 14)
+    o, lse = oracle_mod.attention(q, k, v, 1.0)
+    mean = v.mean(axis=1, keepdims=True)
+    np.testing.assert_allclose(o, np.broadcast_to(mean, o.shape), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(sk), rtol=0, atol=1e-13)
+
+
+def test_equal_k_rows_is_uniform(oracle_mod):
+    b, sq, sk, h, d = 2, 3, 9, 1, 4
+    q = _rand((b, sq, h, d), 15)
+    krow = _rand((b, 1, h, d), 16)
+    k = np.broadcast_to(krow, (b, sk, h, d)).copy()
+    v = _rand((b, sk, h, d), 17)
+    o, lse = oracle_mod.attention(q, k, v, 0.8)
+    mean = v.mean(axis=1, keepdims=True)
+    np.testing.assert_allclose(o, np.broadcast_to(mean, o.shape), rtol=0, atol=1e-13)
+    s0 = 0.8 * np.einsum("bihd,bhd->bhi", q, krow[:, 0])
+    np.testing.assert_allclose(lse, s0 + math.log(sk), rtol=0, atol=1e-13)
+
+
+def test_lse_bounds_and_permutation(oracle_mod):
+    b, sq, sk, h, d = 2, 6, 17, 3, 8
+    q, k, v = _rand((b, sq, h, d), 18) * 2, _rand((b, sk, h, d), 19), _rand((b, sk, h, d), 20)
+    scale = 0.6
+    o, lse = oracle_mod.attention(q, k, v, scale)
+    s = scale * np.einsum("bihd,bjhd->bhij", q, k)
+    smax = s.max(axis=-1)
+    assert np.all(lse >= smax - 1e-12)
+    assert np.all(lse <= smax + math.log(sk) + 1e-12)
+    perm = np.random.default_rng(21).permutation(sk)
+    o2, lse2 = oracle_mod.attention(q, k[:, perm], v[:, perm], scale)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+
+
+def test_identity_v_exposes_probabilities(oracle_mod):
+    """With V = I (sk = d) row i of O is the softmax row P_i: non-negative,
+    summing to one, and proportional to exp(s_ij) with LSE as the log of the
+    normaliser."""
+    b, sq, h = 1, 5, 2
+    sk = d = 7
+    q, k = _rand((b, sq, h, d), 22) * 2, _rand((b, sk, h, d), 23)
+    v = np.zeros((b, sk, h, d))
+    for j in range(sk):
+        v[:, j, :, j] = 1.0
+    scale = 0.9
+    o, lse = oracle_mod.attention(q, k, v, scale)
+    p = o.transpose(0, 2, 1, 3)  # (b, h, sq, sk)
+    assert np.all(p >= 0)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-14)
+    s = scale * np.einsum("bihd,bjhd->bhij", q, k)
+    np.testing.assert_allclose(np.log(p), s - lse[..., None], rtol=0, atol=1e-12)
+
+
+def test_rows_subset_and_key_range(oracle_mod):
+    b, sq, sk, h, d = 2, 9, 12, 2, 4
+    q, k, v = _rand((b, sq, h, d), 24), _rand((b, sk, h, d), 25), _rand((b, sk, h, d), 26)
+    o, lse = oracle_mod.attention(q, k, v, 0.5)
+    rows = [8, 0, 3]
+    o_r, lse_r = oracle_mod.attention(q, k, v, 0.5, rows=rows)
+    np.testing.assert_array_equal(o_r, o[:, rows])
+    np.testing.assert_array_equal(lse_r, lse[:, :, rows])
+    o_k, lse_k = oracle_mod.attention(q, k, v, 0.5, key_range=(3, 10))
+    o_s, lse_s = oracle_mod.attention(q, k[:, 3:10].copy(), v[:, 3:10].copy(), 0.5)
+    np.testing.assert_array_equal(o_k, o_s)
+    np.testing.assert_array_equal(lse_k, lse_s)
+    o_e, lse_e = oracle_mod.attention(q, k, v, 0.5, key_range=(4, 4))
+    assert np.all(o_e == 0) and np.all(np.isneginf(lse_e))
+
+
+@pytest.mark.parametrize("bounds", [
+    [(0, 13)],
+    [(0, 5), (5, 13)],
+    [(0, 1), (1, 2), (2, 7), (7, 13)],
+    [(0, 4), (4, 4), (4, 13), (13, 13)],  # empty splits
+    [(0, 0), (0, 13)],
+])
+def test_split_combine_equals_unsplit(oracle_mod, bounds):
+    b, sq, sk, h, d = 2, 3, 13, 2, 5
+    q, k, v = _rand((b, sq, h, d), 27) * 2, _rand((b, sk, h, d), 28), _rand((b, sk, h, d), 29)
+    o, lse = oracle_mod.attention(q, k, v, 0.77)
+    o2, lse2 = oracle_mod.split_attention(q, k, v, 0.77, bounds)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+
+
+def test_combine_weights_are_the_formula_not_uniform(oracle_mod):
+    """Unequal split sizes make a plain average of O_i wrong; the reduce must
+    weight each split by exp(LSE_i - LSE)."""
+    b, sq, sk, h, d = 1, 2, 40, 1, 3
+    q, k, v = _rand((b, sq, h, d), 30) * 3, _rand((b, sk, h, d), 31), _rand((b, sk, h, d), 32)
+    parts = [oracle_mod.attention(q, k, v, 1.0, key_range=r) for r in [(0, 3), (3, 40)]]
+    o, _ = oracle_mod.attention(q, k, v, 1.0)
+    avg = 0.5 * (parts[0][0] + parts[1][0])
+    assert np.abs(avg - o).max() > 1e-3
+    o2, _ = oracle_mod.split_attention(q, k, v, 1.0, [(0, 3), (3, 40)])
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- 16-bit decode
+def test_every_f16_pattern(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_mod.decode_f16(int(x)) for x in bits])
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got) & (got > 0), np.isinf(ref) & (ref > 0))
+
+
+def test_every_bf16_pattern(oracle_mod):
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle_mod.decode_bf16(int(x) & 0xFFFF) for x in bits.tolist()])
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_narrow_inputs_match_widened(oracle_mod, dtype):
+    b, sq, sk, h, d = 2, 5, 7, 3, 16
+    g = torch.Generator().manual_seed(0)
+    q, k, v = (torch.randn(s, generator=g).to(dtype) for s in
+               [(b, sq, h, d), (b, sk, h, d), (b, sk, h, d)])
+    o, lse = oracle_mod.attention(q, k, v, 0.25)
+    o64, lse64 = oracle_mod.attention(q.double(), k.double(), v.double(), 0.25)
+    np.testing.assert_array_equal(o, o64)
+    np.testing.assert_array_equal(lse, lse64)

@@ -1,0 +1,203 @@
+"""exact_attention_65_gb300: exact attention on one GB300 through the exattn C ABI.
+
+A thin ctypes binding over ``libexattn.so`` (built by
+``exact_attention_65_gb300.build``). It only checks and marshals arguments:
+every step of the computation runs in the library's CUDA kernels, and there
+is no CPU or framework fallback. PyTorch supplies device memory and the
+current CUDA stream.
+
+    o, lse = attn_fwd(q, k, v)                  # q, k, v: [b, s, h, d] fp16/bf16 CUDA tensors
+    o, lse = attn_decode_splitkv(q, k, v)       # split-KV decode, num_splits=0: heuristic
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libexattn.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "exattn.h")
+
+ATTN_FP16, ATTN_BF16 = 0, 1
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_NO_MEMORY = 4
+ATTN_ERR_DEVICE_TIMEOUT = 5
+ATTN_DEBUG_SKIP_LOADS = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-OK status returned by the C ABI."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libexattn.so; raise if it has not been built (there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m exact_attention_65_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
+        lib.attn_fwd.restype = i32
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_decode_splitkv.restype = i32
+        lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_decode_splitkv_ex.restype = i32
+        lib.attn_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                               i32, i32, vp]
+        lib.attn_decode_num_splits.restype = i32
+        lib.attn_decode_num_splits.argtypes = [i32] * 5
+        lib.attn_decode_num_splits_for_sms.restype = i32
+        lib.attn_decode_num_splits_for_sms.argtypes = [i32] * 6
+        lib.attn_get_device_status.restype = i32
+        lib.attn_get_device_status.argtypes = [vp]
+        lib.attn_last_timeout_site.restype = u32
+        lib.attn_last_timeout_site.argtypes = []
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_release_workspace.restype = None
+        lib.attn_release_workspace.argtypes = []
+        lib.attn_debug_set_flags.restype = None
+        lib.attn_debug_set_flags.argtypes = [u32]
+        lib.attn_version.restype = i32
+        lib.attn_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"exattn takes float16 or bfloat16 tensors, got {t.dtype}")
+
+
+def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [b, s, h, d], got shape {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous in (b, s, h, d) order")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on the same device")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    b, sq, h, d = q.shape
+    if k.shape != v.shape or k.shape[0] != b or k.shape[2] != h or k.shape[3] != d:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    return b, sq, k.shape[1], h, d, _dtype_code(q)
+
+
+def _outputs(q, out, lse, b, h, sq):
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
+    elif (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
+          or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 tensor [b, h, sq]")
+    return out, lse
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=None):
+    """Exact attention O = softmax(scale * Q K^T) V and LSE [b, h, sq] (fp32).
+
+    q: [b, sq, h, d], k/v: [b, sk, h, d], fp16 or bf16, contiguous CUDA
+    tensors; default scale 1/sqrt(d). Runs on ``stream`` (default: the
+    current stream of q's device)."""
+    b, sq, sk, h, d, dt = _check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, b, h, sq)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0, out=None,
+                        lse=None, stream=None):
+    """Split-KV decode: same result as attn_fwd, computed by splitting the
+    keys into ``num_splits`` ranges (0 = heuristic) and reducing the
+    per-split (O_i, LSE_i) with the log-sum-exp combine."""
+    b, sq, sk, h, d, dt = _check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, b, h, sq)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode_splitkv_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr(), b, sq, sk, h, d, scale, int(num_splits), dt,
+                                        _stream(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_splitkv")
+    return out, lse
+
+
+def attn_decode_num_splits(b: int, sq: int, sk: int, h: int, d: int) -> int:
+    """Split count the heuristic picks on the current device."""
+    return load_library().attn_decode_num_splits(b, sq, sk, h, d)
+
+
+def attn_decode_num_splits_for_sms(b: int, sq: int, sk: int, h: int, d: int, num_sms: int) -> int:
+    """Split count the heuristic picks for a device with ``num_sms`` SMs."""
+    return load_library().attn_decode_num_splits_for_sms(b, sq, sk, h, d, num_sms)
+
+
+def attn_get_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device status."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return load_library().attn_get_device_status(_stream(device, stream))
+
+
+def attn_last_timeout_site() -> int:
+    return load_library().attn_last_timeout_site()
+
+
+def attn_release_workspace() -> None:
+    load_library().attn_release_workspace()
+
+
+def attn_debug_set_flags(flags: int) -> None:
+    load_library().attn_debug_set_flags(int(flags))
+
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_num_splits",
+    "attn_decode_num_splits_for_sms", "attn_get_device_status", "attn_last_timeout_site",
+    "attn_release_workspace", "attn_debug_set_flags", "attn_status_string", "load_library",
+]

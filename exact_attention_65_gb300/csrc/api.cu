@@ -1,0 +1,274 @@
+// C-ABI layer of exattn: argument validation, the split heuristic, TMA
+// tensor-map encoding, the decode workspace and the device status word.
+// Declared in include/exattn.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "exattn.h"
+#include "internal.h"
+
+using namespace exattn;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DeviceState {
+    bool ready = false;
+    uint32_t *status = nullptr;  // device word written by kernels that give up a wait
+    int num_sms = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+unsigned int g_flags = 0;
+unsigned int g_last_site = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+attn_status_t device_state(DeviceState **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return ATTN_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        uint32_t *status = nullptr;
+        if (cudaMalloc(&status, 16) != cudaSuccess) return ATTN_ERR_NO_MEMORY;
+        if (cudaMemset(status, 0, 16) != cudaSuccess) {
+            cudaFree(status);
+            return ATTN_ERR_CUDA;
+        }
+        // Keep decode workspace that was handed back cached in the pool
+        // instead of returning it to the system at every synchronisation.
+        cudaMemPool_t pool;
+        if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+            uint64_t keep = UINT64_MAX;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        }
+        st.status = status;
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    *out = &st;
+    return ATTN_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn_status_t validate(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, int b, int sq, int sk, int h, int d, float scale,
+                       int dtype) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (b < 1 || sq < 1 || sk < 1 || h < 1) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (b > 65535 || h > 65535) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// (d, h, s, b) view of a contiguous [b, s, h, d] tensor; box (box0, 1, box2, 1).
+bool encode_4d(CUtensorMap *map, const void *base, bool bf16, int d, int h, int s, int b,
+               int box0, int box2, CUtensorMapSwizzle swizzle) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                                static_cast<cuuint64_t>(s), static_cast<cuuint64_t>(b)};
+    const cuuint64_t row = static_cast<cuuint64_t>(d) * 2;
+    const cuuint64_t strides[3] = {row, row * h, row * h * static_cast<cuuint64_t>(s)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), 1u, static_cast<cuuint32_t>(box2), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = g_encode(
+        map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle fwd_swizzle(int d) {
+    switch (fwd_row_bytes(d)) {
+        case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+        case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+        default: return CU_TENSOR_MAP_SWIZZLE_32B;
+    }
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char *attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported size or head dim";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_NO_MEMORY: return "out of device memory";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    }
+    return "unknown status";
+}
+
+void attn_debug_set_flags(unsigned int flags) { g_flags = flags & ATTN_DEBUG_SKIP_LOADS; }
+
+unsigned int attn_last_timeout_site(void) { return g_last_site; }
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b,
+                       int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+    attn_status_t st = validate(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    const int box0 = fwd_row_bytes(d) / 2;
+    CUtensorMap tq, tk, tv;
+    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, FWD_BM, fwd_swizzle(d)) ||
+        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)) ||
+        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)))
+        return ATTN_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.b = b;
+    a.sq = sq;
+    a.sk = sk;
+    a.h = h;
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = g_flags;
+    return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms) {
+    if (b < 1 || sq < 1 || sk < 1 || h < 1 || num_sms < 1) return 0;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
+    const int64_t units = static_cast<int64_t>(b) * h * cdiv(sq, dec_rows_per_cta(sq));
+    const int64_t nblocks = cdiv(sk, dec_block_rows(d));
+    if (units >= num_sms) return 1;  // every SM already has work: no reason to split
+    // Otherwise aim at two CTAs per SM (two decode CTAs fit in one SM's
+    // shared memory), without making splits smaller than one key block.
+    int64_t s = cdiv(2 * static_cast<int64_t>(num_sms), units);
+    if (s > nblocks) s = nblocks;
+    if (s > 128) s = 128;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int attn_decode_num_splits(int b, int sq, int sk, int h, int d) {
+    DeviceState *ds = nullptr;
+    if (device_state(&ds) != ATTN_OK) return 0;
+    return attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms);
+}
+
+attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v, void *o,
+                                     float *lse, int b, int sq, int sk, int h, int d, float scale,
+                                     int num_splits, attn_dtype_t dtype, cudaStream_t stream) {
+    attn_status_t st = validate(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(b) * cdiv(sq, dec_rows_per_cta(sq)) > 65535) return ATTN_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    const int64_t nblocks = cdiv(sk, dec_block_rows(d));
+    int64_t splits = num_splits == 0
+                         ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms)
+                         : num_splits;
+    if (splits > nblocks) splits = nblocks;
+    if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
+    if (splits < 1) splits = 1;
+
+    CUtensorMap tk, tv;
+    if (!encode_4d(&tk, k, bf16, d, h, sk, b, d, dec_box_rows(d), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_4d(&tv, v, bf16, d, h, sk, b, d, dec_box_rows(d), CU_TENSOR_MAP_SWIZZLE_NONE))
+        return ATTN_ERR_CUDA;
+
+    DecodeArgs a;
+    a.q = q;
+    a.o = o;
+    a.lse = lse;
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    a.b = b;
+    a.sq = sq;
+    a.sk = sk;
+    a.h = h;
+    a.splits = static_cast<int>(splits);
+    a.blocks_per_split = static_cast<int>(cdiv(nblocks, splits));
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = g_flags;
+
+    if (splits == 1)
+        return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+
+    const int64_t rows = static_cast<int64_t>(b) * sq * h;
+    const size_t o_bytes = static_cast<size_t>(splits * rows * d) * sizeof(float);
+    const size_t l_bytes = static_cast<size_t>(splits * rows) * sizeof(float);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, o_bytes + l_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_MEMORY;
+    }
+    a.o_part = static_cast<float *>(ws);
+    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes);
+    cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
+    if (e == cudaSuccess)
+        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int b, int sq, int sk, int h, int d, float scale, int num_splits,
+                                  cudaStream_t stream) {
+    return attn_decode_splitkv_ex(q, k, v, o, lse, b, sq, sk, h, d, scale, num_splits, ATTN_BF16,
+                                  stream);
+}
+
+attn_status_t attn_get_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    DeviceState *ds = nullptr;
+    if (device_state(&ds) != ATTN_OK) return ATTN_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (word != 0) {
+        g_last_site = word;
+        if (cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;
+        return ATTN_ERR_DEVICE_TIMEOUT;
+    }
+    return ATTN_OK;
+}
+
+void attn_release_workspace(void) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+        cudaDeviceSynchronize();
+        cudaMemPoolTrimTo(pool, 0);
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,454 @@
+// Forward exact attention on sm_103a: TMA-staged Q/K/V tiles, S = Q K^T and
+// O += P V as tcgen05 MMAs accumulating in tensor memory, and an online
+// softmax with one thread per query row.
+//
+// What is computed follows "Why FlashAttention is fast": the score matrix
+// is cut into tiles (section 3.1), the whole QK^T -> softmax -> PV chain
+// runs in one kernel with the intermediates on chip (section 3.2), and the
+// softmax is done online: a running max and running sum per row, with the
+// partial output rescaled whenever the reference max moves (section 3.3).
+// The per-row log-sum-exp is emitted beside O.
+//
+// CTA layout (384 threads, one CTA per SM):
+//   warp 0        TMA producer: Q tiles once, then K_j and V_j through a
+//                 ring of STAGES slots each.
+//   warp 1        TMEM owner and MMA issuer (one thread): S_j(t) = Q_t K_j^T
+//                 into TMEM, then O_t += P_j(t) V_j with P read from TMEM.
+//   warps 2-3     idle (kept so the softmax warps start at a warpgroup
+//                 boundary, which the TMEM lane quarters require).
+//   warps 4-7     softmax for query tile 0, warps 8-11 for query tile 1:
+//                 thread i owns row i of its tile (TMEM lane i).
+// The two query tiles ping-pong: while one warpgroup exponentiates its S
+// tile, the tensor core works on the other tile's MMAs.
+//
+// TMEM (512 columns, fp32): tile t uses columns [256t, 256t+128) for S_j,
+// overwritten in place by P_j packed two 16-bit values per column, and
+// [256t+128, 256t+128+d) for the O accumulator.
+//
+// Lazy rescaling: a row keeps its reference max m until a tile's max
+// exceeds it by more than 8 (log2 units). P = 2^(s*c - m) then stays at most
+// 2^8, which fp16/bf16 and the fp32 sums hold exactly as well as values
+// below 1; the final O/l and LSE = m + log2(l) are the same quantity.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace exattn {
+namespace {
+
+template <int D>
+struct FwdGeom {
+    static constexpr int BM = FWD_BM;
+    static constexpr int BN = FWD_BN;
+    static constexpr int QT = FWD_QTILES;
+    static constexpr int ROW_BYTES = fwd_row_bytes(D);
+    static constexpr int PANELS = (D * 2) / ROW_BYTES;
+    static constexpr int PANEL_ELEMS = ROW_BYTES / 2;
+    static constexpr int Q_PANEL_BYTES = BM * ROW_BYTES;
+    static constexpr int KV_PANEL_BYTES = BN * ROW_BYTES;
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
+    static constexpr int KV_TILE_BYTES = BN * D * 2;
+    static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    static constexpr uint32_t LAYOUT =
+        ROW_BYTES == 128 ? kLayoutSw128 : (ROW_BYTES == 64 ? kLayoutSw64 : kLayoutSw32);
+    static constexpr uint32_t SBO = 8 * ROW_BYTES;  // bytes between 8-row core-matrix groups
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_TILE_STRIDE = 256;
+    static constexpr int TMEM_O_OFF = 128;
+    static constexpr int OCH = D < 32 ? D : 32;  // O columns per TMEM load in the epilogue
+
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + QT * Q_TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE_BYTES;
+    // barriers: q | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] | s_full[QT] | p_full[QT] |
+    //           o_full[QT] | done
+    static constexpr int BAR_Q = 0;
+    static constexpr int BAR_KF = 1;
+    static constexpr int BAR_KE = BAR_KF + STAGES;
+    static constexpr int BAR_VF = BAR_KE + STAGES;
+    static constexpr int BAR_VE = BAR_VF + STAGES;
+    static constexpr int BAR_SF = BAR_VE + STAGES;
+    static constexpr int BAR_PF = BAR_SF + QT;
+    static constexpr int BAR_OF = BAR_PF + QT;
+    static constexpr int BAR_DONE = BAR_OF + QT;
+    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int USED = OFF_MISC + 16;
+    // Keep one CTA per SM: it owns all 512 TMEM columns.
+    static constexpr int MIN_SMEM = 120 * 1024;
+    static constexpr int SMEM_BYTES = (USED > MIN_SMEM ? USED : MIN_SMEM) + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(D % 16 == 0 && D >= 16 && D <= 128, "head dim");
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
+                                             const CUtensorMap *tv, uint32_t sbase, int head,
+                                             int batch, int m0, int n_qt, int nkv,
+                                             const WaitGuard &g) {
+    using G = FwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    const uint64_t keep = policy_evict_last();  // K/V are re-read by every query block of the head
+
+    mbar_arrive_expect_tx(bar(G::BAR_Q), n_qt * G::Q_TILE_BYTES);
+    for (int t = 0; t < n_qt; ++t)
+        for (int p = 0; p < G::PANELS; ++p)
+            tma_load_4d(sbase + G::OFF_Q + t * G::Q_TILE_BYTES + p * G::Q_PANEL_BYTES, tq,
+                        bar(G::BAR_Q), p * G::PANEL_ELEMS, head, m0 + t * G::BM, batch);
+
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < nkv; ++j) {
+        const int s = j % G::STAGES;
+        const uint32_t ph = (j / G::STAGES) & 1;
+        if (!mbar_wait(bar(G::BAR_KE + s), ph ^ 1, g, 1)) break;
+        mbar_arrive_expect_tx(bar(G::BAR_KF + s), G::KV_TILE_BYTES);
+        for (int p = 0; p < G::PANELS; ++p)
+            tma_load_4d_hint(sbase + G::OFF_K + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES, tk,
+                             bar(G::BAR_KF + s), p * G::PANEL_ELEMS, head, j * G::BN, batch, keep);
+        ++k_issued;
+        if (!mbar_wait(bar(G::BAR_VE + s), ph ^ 1, g, 2)) break;
+        mbar_arrive_expect_tx(bar(G::BAR_VF + s), G::KV_TILE_BYTES);
+        for (int p = 0; p < G::PANELS; ++p)
+            tma_load_4d_hint(sbase + G::OFF_V + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES, tv,
+                             bar(G::BAR_VF + s), p * G::PANEL_ELEMS, head, j * G::BN, batch, keep);
+        ++v_issued;
+    }
+    // Never leave the CTA with a copy still landing in shared memory: wait
+    // (bounded, even after an abort) for the last load issued into each slot.
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(bar(G::BAR_Q), 0, drain, 9);
+    for (int j = (k_issued > G::STAGES ? k_issued - G::STAGES : 0); j < k_issued; ++j)
+        mbar_wait(bar(G::BAR_KF + j % G::STAGES), (j / G::STAGES) & 1, drain, 10);
+    for (int j = (v_issued > G::STAGES ? v_issued - G::STAGES : 0); j < v_issued; ++j)
+        mbar_wait(bar(G::BAR_VF + j % G::STAGES), (j / G::STAGES) & 1, drain, 11);
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int n_qt, int nkv,
+                                        const WaitGuard &g) {
+    using G = FwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    constexpr uint32_t idesc_s = mma_idesc_f16(G::BM, G::BN, BF16, false, false);
+    constexpr uint32_t idesc_o = mma_idesc_f16(G::BM, D, BF16, false, true);
+
+    if (mbar_wait(bar(G::BAR_Q), 0, g, 3)) {
+        for (int j = 0; j <= nkv; ++j) {
+            if (j < nkv && !mbar_wait(bar(G::BAR_KF + j % G::STAGES), (j / G::STAGES) & 1, g, 4))
+                break;
+            if (j > 0 &&
+                !mbar_wait(bar(G::BAR_VF + (j - 1) % G::STAGES), ((j - 1) / G::STAGES) & 1, g, 5))
+                break;
+            tc_fence_after();
+            bool ok = true;
+            for (int t = 0; t < n_qt; ++t) {
+                const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE;
+                const uint32_t tO = tS + G::TMEM_O_OFF;
+                if (j > 0) {
+                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8 columns.
+                    if (!mbar_wait(bar(G::BAR_PF + t), (j - 1) & 1, g, 6)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vb = sbase + G::OFF_V + ((j - 1) % G::STAGES) * G::KV_TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < G::BN / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc(vb + kk * 16 * G::ROW_BYTES,
+                                                         G::KV_PANEL_BYTES, G::SBO, G::LAYOUT);
+                        mma_ts(tO, tS + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (j < nkv) {
+                    // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
+                    const uint32_t qb = sbase + G::OFF_Q + t * G::Q_TILE_BYTES;
+                    const uint32_t kb = sbase + G::OFF_K + (j % G::STAGES) * G::KV_TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int p = (kk * 16) / G::PANEL_ELEMS;
+                        const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
+                        const uint64_t adesc =
+                            smem_desc(qb + p * G::Q_PANEL_BYTES + off, 16, G::SBO, G::LAYOUT);
+                        const uint64_t bdesc =
+                            smem_desc(kb + p * G::KV_PANEL_BYTES + off, 16, G::SBO, G::LAYOUT);
+                        mma_ss(tS, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(G::BAR_SF + t));
+                } else {
+                    mma_commit(bar(G::BAR_OF + t));
+                }
+            }
+            if (!ok) break;
+            if (j > 0) mma_commit(bar(G::BAR_VE + (j - 1) % G::STAGES));
+            if (j < nkv) mma_commit(bar(G::BAR_KE + j % G::STAGES));
+        }
+    }
+    // No MMA may still be running when TMEM is released.
+    mma_commit(bar(G::BAR_DONE));
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4,
+                                            int head, int batch, int m0, int nkv, const FwdArgs &a,
+                                            const WaitGuard &g) {
+    using G = FwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    const uint32_t lane = threadIdx.x & 31;
+    const int row = q4 * 32 + lane;
+    const int grow = m0 + t * G::BM + row;
+    const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t tO = tS + G::TMEM_O_OFF;
+    const float c = a.scale_log2;
+    const bool c_pos = c >= 0.f;
+
+    float m_ref = -INFINITY;  // reference max, log2 units
+    float l = 0.f;            // running sum of 2^(s*c - m_ref)
+    bool alive = true;
+
+    for (int j = 0; j < nkv; ++j) {
+        bool ok = mbar_wait(bar(G::BAR_SF + t), j & 1, g, 7);
+        if (!__all_sync(0xffffffffu, ok)) {
+            alive = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t sr[G::BN];
+#pragma unroll
+        for (int c0 = 0; c0 < G::BN; c0 += 32)
+            tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+        tmem_wait_ld();
+        float *s = reinterpret_cast<float *>(sr);
+
+        const int valid = a.sk - j * G::BN;  // keys of this tile inside [0, sk)
+        const bool ragged = valid < G::BN;
+
+        // row max of the scaled scores (min of the raw ones if scale < 0)
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
+        if (!ragged) {
+            if (c_pos) {
+#pragma unroll
+                for (int i = 0; i < G::BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < G::BN; ++i) mx[i & 7] = fminf(mx[i & 7], s[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < G::BN; ++i) {
+                if (i < valid) mx[i & 7] = c_pos ? fmaxf(mx[i & 7], s[i]) : fminf(mx[i & 7], s[i]);
+            }
+        }
+        float mraw = mx[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) mraw = c_pos ? fmaxf(mraw, mx[i]) : fminf(mraw, mx[i]);
+        const float m_tile = mraw * c;
+
+        const bool need = m_tile > m_ref + 8.0f;
+        const float m_new = need ? m_tile : m_ref;
+        const float alpha = fast_exp2(m_ref - m_new);  // 1 if kept, 0 on the first tile
+        m_ref = m_new;
+
+        // P = 2^(s*c - m_ref), packed in pairs into the S columns.
+        const float neg_m = -m_ref;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[G::BN / 2];
+#pragma unroll
+        for (int i = 0; i < G::BN / 2; ++i) {
+            float p0 = fast_exp2(fmaf(s[2 * i], c, neg_m));
+            float p1 = fast_exp2(fmaf(s[2 * i + 1], c, neg_m));
+            if (ragged) {
+                p0 = (2 * i < valid) ? p0 : 0.f;
+                p1 = (2 * i + 1 < valid) ? p1 : 0.f;
+            }
+            ls[i & 3] += p0 + p1;
+            pk[i] = pack2<BF16>(p0, p1);
+        }
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+#pragma unroll
+        for (int c0 = 0; c0 < G::BN / 2; c0 += 32)
+            tmem_st32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&pk[c0]));
+
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // O row *= alpha; PV_{j-1} has completed (S_j's commit covers it).
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += G::OCH) {
+                if constexpr (G::OCH == 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c0, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(tO + c0, ov);
+                } else {
+                    uint32_t ov[16];
+                    tmem_ld16(tO + c0, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st16(tO + c0, ov);
+                }
+            }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
+    }
+
+    if (!alive) return;
+    bool ok = mbar_wait(bar(G::BAR_OF + t), 0, g, 8);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    tc_fence_after();
+
+    const float inv_l = 1.0f / l;
+    const bool in_range = grow < a.sq;
+    using Elem = uint16_t;
+    Elem *orow = reinterpret_cast<Elem *>(a.o) +
+                 ((static_cast<int64_t>(batch) * a.sq + grow) * a.h + head) * D;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += G::OCH) {
+        uint32_t ov[G::OCH];
+        if constexpr (G::OCH == 32)
+            tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(ov));
+        else
+            tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
+        tmem_wait_ld();
+        uint32_t packed[G::OCH / 2];
+#pragma unroll
+        for (int i = 0; i < G::OCH / 2; ++i)
+            packed[i] = pack2<BF16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
+        if (in_range) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+            for (int i = 0; i < G::OCH / 8; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+        }
+    }
+    if (in_range)
+        a.lse[(static_cast<int64_t>(batch) * a.h + head) * a.sq + grow] =
+            (m_ref + __log2f(l)) * 0.69314718055994530942f;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(FWD_THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+    using G = FwdGeom<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const int head = blockIdx.y, batch = blockIdx.z;
+    const int m0 = blockIdx.x * (G::BM * G::QT);
+    const int n_qt = min(G::QT, (a.sq - m0 + G::BM - 1) / G::BM);
+    const int nkv = (a.sk + G::BN - 1) / G::BN;
+
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + G::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < G::NUM_BARS; ++i) {
+            uint32_t count = 1;
+            if (i >= G::BAR_PF && i < G::BAR_PF + G::QT) count = 4;  // one arrive per softmax warp
+            mbar_init(bar(i), count);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitGuard g{abort_flag, a.status, kKernFwd};
+
+    if (warp == 0) {
+        if (lane == 0 && !(a.flags & kFlagSkipLoads))
+            fwd_producer<D>(&tq, &tk, &tv, sbase, head, batch, m0, n_qt, nkv, g);
+    } else if (warp == 1) {
+        if (lane == 0) fwd_mma<D, BF16>(sbase, tmem, n_qt, nkv, g);
+    } else if (warp >= 4) {
+        const int t = (warp - 4) >> 2;
+        if (t < n_qt) fwd_softmax<D, BF16>(sbase, tmem, t, warp & 3, head, batch, m0, nkv, a, g);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const FwdArgs &a, cudaStream_t stream) {
+    using G = FwdGeom<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 G::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid((a.sq + G::BM * G::QT - 1) / (G::BM * G::QT), a.h, a.b);
+    fwd_kernel<D, BF16><<<grid, FWD_THREADS, G::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const FwdArgs &a, cudaStream_t stream) {
+#define EXATTN_FWD_CASE(DD)                                               \
+    case DD:                                                              \
+        return bf16 ? launch_fwd_t<DD, true>(tq, tk, tv, a, stream)       \
+                    : launch_fwd_t<DD, false>(tq, tk, tv, a, stream);
+    switch (d) {
+        EXATTN_FWD_CASE(16)
+        EXATTN_FWD_CASE(32)
+        EXATTN_FWD_CASE(64)
+        EXATTN_FWD_CASE(128)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef EXATTN_FWD_CASE
+}
+
+}  // namespace exattn

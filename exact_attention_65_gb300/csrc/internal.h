@@ -1,0 +1,66 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace exattn {
+
+// ------------------------------------------------------------ forward
+// One CTA owns FWD_QTILES query tiles of FWD_BM rows of one (batch, head)
+// and streams the keys in tiles of FWD_BN rows.
+constexpr int FWD_BM = 128;
+constexpr int FWD_BN = 128;
+constexpr int FWD_QTILES = 2;
+constexpr int FWD_THREADS = 384;
+
+// Bytes of one swizzled smem row of a tile (the TMA box's inner extent):
+// d*2 for d <= 64 (32/64/128-byte swizzle), 128 for d = 128 (two panels).
+constexpr int fwd_row_bytes(int d) { return d * 2 < 128 ? d * 2 : 128; }
+
+struct FwdArgs {
+    void *o;
+    float *lse;
+    int b, sq, sk, h;
+    float scale_log2;  // scale * log2(e)
+    uint32_t *status;
+    uint32_t flags;
+};
+
+cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const FwdArgs &a, cudaStream_t stream);
+
+// ------------------------------------------------------------ decode
+// Keys are streamed in blocks of 16 KB per tensor (dec_block_rows(d) rows).
+constexpr int DEC_BLOCK_BYTES = 16384;
+constexpr int DEC_MAX_SPLITS = 1024;
+constexpr int dec_block_rows(int d) { return DEC_BLOCK_BYTES / (d * 2); }
+constexpr int dec_box_rows(int d) { return dec_block_rows(d) < 256 ? dec_block_rows(d) : 256; }
+// Query rows handled by one CTA.
+inline int dec_rows_per_cta(int sq) { return sq == 1 ? 1 : 4; }
+
+struct DecodeArgs {
+    const void *q;
+    void *o;          // final output when splits == 1
+    float *lse;       // final LSE when splits == 1
+    float *o_part;    // [splits, b, sq, h, d] when splits > 1
+    float *lse_part;  // [splits, b, h, sq] when splits > 1
+    int b, sq, sk, h;
+    int splits;
+    int blocks_per_split;
+    float scale_log2;
+    uint32_t *status;
+    uint32_t flags;
+};
+
+cudaError_t launch_decode(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeArgs &a, cudaStream_t stream);
+
+cudaError_t launch_combine(int d, bool bf16, const float *o_part, const float *lse_part, void *o,
+                           float *lse, int b, int sq, int h, int splits, cudaStream_t stream);
+
+constexpr uint32_t kFlagSkipLoads = 1u;
+
+}  // namespace exattn

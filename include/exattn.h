@@ -1,0 +1,127 @@
+/*
+ * exattn -- exact scaled-dot-product attention on one GB300 (sm_103a).
+ *
+ * C ABI. Every entry point takes plain pointers and sizes; no C++ or
+ * framework types cross it and no exception leaves it.
+ *
+ * Common conventions
+ *   Layout   q, o: [b, sq, h, d]; k, v: [b, sk, h, d]; contiguous, d
+ *            innermost (the (b, s, h, d) layout "Why FlashAttention is
+ *            fast" section 2 item 2 says flash_attn_func consumes directly,
+ *            so no transposes are needed). lse: [b, h, sq], fp32.
+ *   Memory   q, k, v, o, lse are DEVICE pointers on the current CUDA device,
+ *            owned by the caller; the library never frees or keeps them.
+ *            q, k, v, o must be 16-byte aligned, lse 4-byte aligned.
+ *   Streams  every compute call is asynchronous on `stream` (0 = legacy
+ *            default stream). Argument errors are returned before anything
+ *            is enqueued. A wait inside a kernel that exceeds its bound
+ *            (about two seconds) ends the kernel early and records a device
+ *            status word; attn_get_device_status() reports it.
+ *   Math     O = softmax(scale * Q K^T) V row by row, with fp32 accumulation
+ *            and an online (running max / running sum) softmax, so the
+ *            score matrix never reaches global memory ("Why FlashAttention
+ *            is fast", sections 3.1-3.3). LSE[b, h, i] = ln sum_j
+ *            exp(scale * q_i . k_j), natural log, of the scaled scores.
+ *            O is rounded to nearest even into the input dtype.
+ *   Sizes    b, sq, sk, h >= 1; d in {16, 32, 64, 128}; scale finite
+ *            (0 and negative values are accepted). b and h at most 65535.
+ */
+#ifndef EXATTN_H
+#define EXATTN_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, size < 1, non-finite scale, bad dtype */
+    ATTN_ERR_UNSUPPORTED = 2,    /* d outside {16, 32, 64, 128}, or a size beyond the grid limits */
+    ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed (launch, tensor-map encode, ...) */
+    ATTN_ERR_NO_MEMORY = 4,      /* the decode workspace could not be allocated */
+    ATTN_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up on a bounded wait (see attn_get_device_status) */
+} attn_status_t;
+
+/*
+ * Forward attention: O and LSE for every query row.
+ * Defined by "Why FlashAttention is fast" section 2 item 4 (S = Q K^T * scale,
+ * softmax, times V; the call flash_attn_func(q, k, v) of item 5), computed
+ * tile by tile with the online softmax of section 3.3. Non-causal, no
+ * dropout. dtype selects fp16 or bf16 for q, k, v and o.
+ * Returns ATTN_OK once the kernel is enqueued on `stream`.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int b, int sq, int sk, int h, int d, float scale,
+                       attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Split-KV decode, bf16 q/k/v/o ("where is flash decoding second stage
+ * (reduce) code?" issue). seqlen_k is cut into num_splits ranges of whole
+ * key blocks; split i writes its own O_i and LSE_i (fp32, library
+ * workspace), and a reduce kernel forms, with the max LSE taken out first,
+ *     LSE = log(sum_i exp(LSE_i)),   O = sum_i exp(LSE_i - LSE) * O_i.
+ * num_splits = 0 lets attn_decode_num_splits() choose; a positive value is
+ * clamped to the number of key blocks. With one split the first kernel
+ * writes O and LSE directly and no workspace is used. Any sq >= 1 is
+ * accepted (non-causal). The workspace is taken stream-ordered from the
+ * device's default memory pool and returned after the reduce; it is kept
+ * cached in the pool until attn_release_workspace().
+ */
+attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int b, int sq, int sk, int h, int d, float scale,
+                                  int num_splits, cudaStream_t stream);
+
+/* attn_decode_splitkv with an explicit dtype (fp16 or bf16). */
+attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                     int b, int sq, int sk, int h, int d, float scale,
+                                     int num_splits, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * The split heuristic for num_splits = 0 on the current device (same issue:
+ * split only when the b * h * ceil(sq / rows per CTA) work units leave SMs
+ * idle). Returns the split count (>= 1), or 0 on invalid sizes or when no
+ * device can be queried.
+ */
+int attn_decode_num_splits(int b, int sq, int sk, int h, int d);
+
+/* The same heuristic for an explicit SM count; pure host arithmetic. */
+int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms);
+
+/*
+ * Synchronises `stream`, then reports and clears the current device's
+ * status word: ATTN_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait
+ * since the last call, ATTN_ERR_CUDA if the stream reported an error,
+ * ATTN_OK otherwise.
+ */
+attn_status_t attn_get_device_status(cudaStream_t stream);
+
+/* Where the last recorded timeout happened (kernel and wait site code), 0 if none. */
+unsigned int attn_last_timeout_site(void);
+
+/* Static, human-readable name of a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/* Returns cached decode workspace memory of the current device to the system. */
+void attn_release_workspace(void);
+
+/*
+ * Test hook for the bounded waits. ATTN_DEBUG_SKIP_LOADS makes the next
+ * launched kernels issue no loads at all, so their first wait runs out and
+ * they return with a timeout status instead of hanging. 0 restores normal
+ * operation. Host-side only; never needed in production.
+ */
+#define ATTN_DEBUG_SKIP_LOADS 1u
+void attn_debug_set_flags(unsigned int flags);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXATTN_H */

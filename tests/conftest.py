@@ -3,9 +3,11 @@ import sys
 
 import pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+TESTS = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(TESTS)
+for p in (ROOT, TESTS):
+    if p not in sys.path:
+        sys.path.insert(0, p)
 
 
 def pytest_configure(config):
@@ -18,3 +20,28 @@ def oracle_mod():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def exattn_lib():
+    """The built C library (compiled here if stale); no GPU needed to load it."""
+    from exact_attention_65_gb300 import build
+
+    build.build()
+    import exact_attention_65_gb300 as ea
+
+    return ea.load_library()
+
+
+@pytest.fixture(scope="session")
+def gpu(exattn_lib):
+    """The CUDA path: the library plus a visible device. Fails (never skips)
+    when no GPU is present, so a GPU run cannot pass vacuously."""
+    import torch
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("GPU tests need a CUDA device")
+    import exact_attention_65_gb300 as ea
+
+    torch.cuda.init()
+    return ea

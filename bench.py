@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic
+input, on one GPU:
+  * forward: b4 s512 h32 d128 bf16 (the problem timed in "Why
+    FlashAttention is fast"), O and LSE, one kernel;
+  * split-KV decode: b1 h16 sk32768 d128 bf16 (the small-batch decode of
+    the flash-decoding issue), heuristic split count, split kernel plus the
+    LSE-combine kernel.
+Headline: forward TFLOP/s (4*b*h*sq*sk*d per call); decode is reported as
+HBM GB/s beside it. Inputs are resident in HBM when the timed region starts;
+L2 is flushed (a 512 MiB write) before every timed kernel. Each kernel is
+timed with CUDA events on the stream it runs on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torchrun, one process per GPU) every rank runs the
+same problem on its own GPU: the path has no exchange step, so the ranks are
+independent replicas; ``value`` is the work of all ranks over the slowest
+rank's time. ``--impl reference`` times the fp64 CPU oracle instead, on a
+bounded sample of the same forward problem, on rank 0's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fwd attention TFLOP/s (b4 s512 h32 d128 bf16); split-KV decode HBM GB/s"
+FWD = workloads.WORKLOADS["mid_fwd"]
+DEC = workloads.WORKLOADS["decode_b1_h16_sk32768"]
+# The pages' own figure for this forward problem: ~9.7 ms per flash_attn_func
+# call, 17.18 GFLOP, i.e. about 1.77 TFLOP/s (wall clock, unspecified GPU).
+PAGE_FWD_TFLOPS = 1.77
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CONFIG = {
+    "workload": "fwd b4 s512 h32 d128 bf16 + split-KV decode b1 h16 sk32768 d128 bf16",
+    "fwd": {"b": FWD.b, "sq": FWD.sq, "sk": FWD.sk, "h": FWD.h, "d": FWD.d, "dtype": "bf16",
+            "causal": False},
+    "decode": {"b": DEC.b, "sq": DEC.sq, "sk": DEC.sk, "h": DEC.h, "d": DEC.d, "dtype": "bf16",
+               "num_splits": "heuristic"},
+    "l2": "flushed (512 MiB write) before every timed kernel",
+    "inputs": "seeded N(0,1), torch.Generator seed 42, fp32 draw rounded to bf16",
+    "parallelism": "replicas (no exchange step)",
+}
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, ws, local
+
+
+def dist_init(backend: str):
+    rank, ws, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, ws
+
+
+def aggregate(local_ms: dict, local_units: dict) -> tuple[dict, dict]:
+    """Max of each timing and sum of each work count over all ranks (identity
+    on one rank)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return dict(local_ms), dict(local_units)
+    dev = torch.device("cuda", torch.cuda.current_device()) if (
+        dist.get_backend() == "nccl") else torch.device("cpu")
+    keys_t, keys_u = sorted(local_ms), sorted(local_units)
+    t = torch.tensor([local_ms[k] for k in keys_t], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units[k] for k in keys_u], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return ({k: float(x) for k, x in zip(keys_t, t.tolist())},
+            {k: float(x) for k, x in zip(keys_u, u.tolist())})
+
+
+def barrier():
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks / profiles
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("exact_attention_65_gb300/csrc/fwd.cu", "exact_attention_65_gb300/csrc/decode.cu",
+                "exact_attention_65_gb300/csrc/ptx.cuh", "exact_attention_65_gb300/csrc/internal.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha256") != kernel_source_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100", "-f", self.path]
+            if self.uuid:
+                cmd[1:1] = ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.4)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        power = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ our arm
+def place(w, dev, pin=False):
+    q, k, v = workloads.make_workload(w, pin=pin)
+    return (q, k, v), tuple(t.to(dev, non_blocking=False) for t in (q, k, v))
+
+
+def time_loop(fns, steps, warmup, flush, stream):
+    """Run `fns` (list of callables) per step, each preceded by an L2 flush
+    and bracketed by events; return mean ms per callable and the wall s."""
+    for _ in range(warmup):
+        for fn in fns:
+            flush()
+            fn()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in fns] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        for j, fn in enumerate(fns):
+            flush()
+            ev[i][j][0].record(stream)
+            fn()
+            ev[i][j][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    ms = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(steps)) / steps
+          for j in range(len(fns))]
+    return ms, wall
+
+
+def cpu_baseline(host_qkv, seconds: float = 8.0):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the forward
+    problem: R query rows of every (b, h), R chosen for about `seconds`."""
+    import oracle
+
+    oracle.build()
+    q, k, v = host_qkv
+    per_row_flops = 4 * FWD.sk * FWD.d * FWD.b * FWD.h
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, FWD.scale, rows=list(range(4)))
+    t_probe = max(time.perf_counter() - t0, 1e-4)
+    rows_n = int(min(FWD.sq, max(4, 4 * seconds / t_probe)))
+    rows = list(range(0, FWD.sq, max(1, FWD.sq // rows_n)))[:rows_n]
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, FWD.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": per_row_flops * len(rows) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle on {len(rows)} of {FWD.sq} query rows of every (b, h) of "
+                      f"b4 s512 h32 d128 ({dt:.1f} s)"}
+
+
+def run_ours(args):
+    import exact_attention_65_gb300 as ea
+
+    rank, ws, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    ea.load_library()
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+
+    (hq, hk, hv), (q, k, v) = place(FWD, dev, pin=True)
+    _, (dq, dk, dv) = place(DEC, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(FWD.b, FWD.h, FWD.sq, dtype=torch.float32, device=dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty(DEC.b, DEC.h, DEC.sq, dtype=torch.float32, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    splits = ea.attn_decode_num_splits(DEC.b, DEC.sq, DEC.sk, DEC.h, DEC.d)
+
+    def fwd():
+        ea.attn_fwd(q, k, v, scale=FWD.scale, out=o, lse=lse)
+
+    def dec():
+        ea.attn_decode_splitkv(dq, dk, dv, scale=DEC.scale, num_splits=0, out=do, lse=dlse)
+
+    if ea.attn_get_device_status() != ea.ATTN_OK:
+        raise RuntimeError("device status not clean before the benchmark")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
+    sampler.start()
+    (fwd_ms, dec_ms), wall = time_loop([fwd, dec], args.steps, args.warmup, flush, stream)
+    clocks = sampler.stop()
+    if ea.attn_get_device_status() != ea.ATTN_OK:
+        raise RuntimeError("a kernel reported a timeout during the timed region")
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e_steps = min(args.steps, 200)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    eq, ek, ev_ = (torch.empty_like(t) for t in (q, k, v))
+
+    def e2e_step():
+        eq.copy_(hq, non_blocking=True)
+        ek.copy_(hk, non_blocking=True)
+        ev_.copy_(hv, non_blocking=True)
+        oo, ll = ea.attn_fwd(eq, ek, ev_, scale=FWD.scale)
+        ho.copy_(oo, non_blocking=True)
+        hl.copy_(ll, non_blocking=True)
+
+    (e2e_ms,), _ = time_loop([e2e_step], e2e_steps, 3, lambda: None, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    times, units = aggregate(
+        {"fwd_ms": fwd_ms, "dec_ms": dec_ms, "e2e_ms": e2e_ms, "wall_s": wall},
+        {"fwd_flops": FWD.flops, "dec_bytes": DEC.io_bytes})
+    n = ws
+    fwd_tflops = units["fwd_flops"] / (times["fwd_ms"] * 1e-3) / 1e12
+    dec_gbs = units["dec_bytes"] / (times["dec_ms"] * 1e-3) / 1e9
+    per_rank_fwd_tflops = FWD.flops / (fwd_ms * 1e-3) / 1e12
+    per_rank_dec_gbs = DEC.io_bytes / (dec_ms * 1e-3) / 1e9
+    e2e_tflops = units["fwd_flops"] / (times["e2e_ms"] * 1e-3) / 1e12
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras = measure_extras(ea, dev, flush, stream, peaks)
+    cpu = cpu_baseline((hq, hk, hv)) if (rank == 0 and ws == 1 and not args.no_cpu) else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(fwd_tflops, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(times["fwd_ms"] + times["dec_ms"], 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(fwd_tflops / PAGE_FWD_TFLOPS, 2),
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": CONFIG,
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "splits": splits,
+                   "ms": round(times["dec_ms"], 5)},
+        "fwd_ms": round(times["fwd_ms"], 5),
+        "wall_ms_per_step_incl_flush": round(times["wall_s"] * 1e3 / args.steps, 4),
+        "roofline": {"bound": "tensor", "achieved": round(per_rank_fwd_tflops, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(per_rank_fwd_tflops / peaks["bf16_tflops"], 4),
+                     "traffic": ncu_traffic("fwd_mid"), "peak_source": peak_src,
+                     "kernel": "fwd_kernel<128, bf16>", "algorithmic_per_launch": FWD.flops},
+        "roofline_decode": {"bound": "hbm", "achieved": round(per_rank_dec_gbs, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(per_rank_dec_gbs / peaks["hbm_gbs"], 4),
+                            "traffic": ncu_traffic("decode_b1"), "peak_source": peak_src,
+                            "kernel": "decode_split_kernel<128, 1, bf16> + combine_kernel",
+                            "algorithmic_per_launch": DEC.io_bytes},
+        "e2e": {"value": round(e2e_tflops, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(times["e2e_ms"], 4)},
+        "gpu_launches": args.steps * (1 + (2 if splits > 1 else 1)),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "extras": extras,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier()
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def measure_extras(ea, dev, flush, stream, peaks):
+    """Per-problem kernel times for the other workloads (20 timed calls each)."""
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(workloads.SEED)
+
+    def rand(w):
+        q = torch.randn((w.b, w.sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        k = torch.randn((w.b, w.sk, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        v = torch.randn((w.b, w.sk, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        return q, k, v
+
+    for name in ("tiny_fwd", "small_head_b2_s50", "small_head_b2_s300", "small_head_b512_s150",
+                 "long_fwd"):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        fn = lambda: ea.attn_fwd(q, k, v, scale=w.scale)  # noqa: E731
+        (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+        tf = w.flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                     "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                     "GB/s": round(w.io_bytes / (ms * 1e-3) / 1e9, 1)}
+        del q, k, v
+    for name, split_list in (("decode_b8_h48_sk8192", [0]),
+                             ("decode_b1_h16_sk32768", [0, 1, 2, 4, 8, 16])):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        for s in split_list:
+            fn = lambda: ea.attn_decode_splitkv(q, k, v, scale=w.scale, num_splits=s)  # noqa: E731
+            (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+            gbs = w.io_bytes / (ms * 1e-3) / 1e9
+            out[f"{name}/splits={s}"] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
+                                         "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del q, k, v
+    if ea.attn_get_device_status() != ea.ATTN_OK:
+        raise RuntimeError("a kernel reported a timeout during the extra measurements")
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The fp64 CPU oracle timed on rank 0's host cores, each step a bounded
+    sample of the forward problem."""
+    rank, ws = dist_init("gloo")
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    q, k, v = workloads.make_workload(FWD)
+    per_row_flops = 4 * FWD.sk * FWD.d * FWD.b * FWD.h
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, FWD.scale, rows=[0])
+    t_row = max(time.perf_counter() - t0, 1e-5)
+    budget_s = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    rows_n = int(max(1, min(FWD.sq, budget_s / t_row)))
+    rows = list(range(rows_n))
+    for _ in range(args.warmup):
+        oracle.attention(q, k, v, FWD.scale, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(q, k, v, FWD.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    value = per_row_flops * rows_n * args.steps / dt / 1e12
+    sample = (f"fp64 oracle on {rows_n} of {FWD.sq} query rows of every (b, h) of "
+              "b4 s512 h32 d128 per step")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": CONFIG,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-problem extra timings")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    _, ws, _ = dist_env()
+    if args.gpus != ws and not (args.gpus == 1 and ws == 1):
+        if ws == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 runs under torchrun, one process per GPU")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

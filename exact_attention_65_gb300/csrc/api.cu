@@ -13,67 +13,34 @@
 
 using namespace exattn;
 
+namespace exattn {
+
 namespace {
-
-constexpr int kMaxDevices = 64;
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct DeviceState {
-    bool ready = false;
-    uint32_t *status = nullptr;  // device word written by kernels that give up a wait
-    int num_sms = 0;
-};
-
-DeviceState g_dev[kMaxDevices];
-std::mutex g_mu;
-unsigned int g_flags = 0;
-unsigned int g_last_site = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+unsigned int g_flags = 0;
+}  // namespace
 
-attn_status_t device_state(DeviceState **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    DeviceState &st = g_dev[dev];
-    if (!st.ready) {
-        if (g_encode == nullptr) {
-            void *fn = nullptr;
-            cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || fn == nullptr)
-                return ATTN_ERR_CUDA;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        uint32_t *status = nullptr;
-        if (cudaMalloc(&status, 16) != cudaSuccess) return ATTN_ERR_NO_MEMORY;
-        if (cudaMemset(status, 0, 16) != cudaSuccess) {
-            cudaFree(status);
-            return ATTN_ERR_CUDA;
-        }
-        // Keep decode workspace that was handed back cached in the pool
-        // instead of returning it to the system at every synchronisation.
-        cudaMemPool_t pool;
-        if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
-            uint64_t keep = UINT64_MAX;
-            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        }
-        st.status = status;
-        st.num_sms = sms;
-        st.ready = true;
-    }
-    *out = &st;
-    return ATTN_OK;
+bool load_tensor_map_encoder() {
+    std::lock_guard<std::mutex> lock(g_encode_mu);
+    if (g_encode != nullptr) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
 }
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+unsigned int debug_flags() { return g_flags; }
 
-attn_status_t validate(const void *q, const void *k, const void *v, const void *o,
-                       const float *lse, int b, int sq, int sk, int h, int d, float scale,
-                       int dtype) {
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn_status_t validate_args(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, int b, int sq, int sk, int h, int d, float scale,
+                            int dtype) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return ATTN_ERR_INVALID_ARG;
@@ -99,6 +66,54 @@ bool encode_4d(CUtensorMap *map, const void *base, bool bf16, int d, int h, int 
         const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+}  // namespace exattn
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DeviceState {
+    bool ready = false;
+    uint32_t *status = nullptr;  // device word written by kernels that give up a wait
+    int num_sms = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+unsigned int g_last_site = 0;
+
+attn_status_t device_state(DeviceState **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        if (!load_tensor_map_encoder()) return ATTN_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        uint32_t *status = nullptr;
+        if (cudaMalloc(&status, 16) != cudaSuccess) return ATTN_ERR_NO_MEMORY;
+        if (cudaMemset(status, 0, 16) != cudaSuccess) {
+            cudaFree(status);
+            return ATTN_ERR_CUDA;
+        }
+        // Keep decode workspace that was handed back cached in the pool
+        // instead of returning it to the system at every synchronisation.
+        cudaMemPool_t pool;
+        if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+            uint64_t keep = UINT64_MAX;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        }
+        st.status = status;
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    *out = &st;
+    return ATTN_OK;
 }
 
 CUtensorMapSwizzle fwd_swizzle(int d) {
@@ -136,7 +151,7 @@ unsigned int attn_last_timeout_site(void) { return g_last_site; }
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b,
                        int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
                        cudaStream_t stream) {
-    attn_status_t st = validate(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
@@ -156,7 +171,7 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     a.h = h;
     a.scale_log2 = scale * kLog2e;
     a.status = ds->status;
-    a.flags = g_flags;
+    a.flags = debug_flags();
     return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -183,7 +198,7 @@ int attn_decode_num_splits(int b, int sq, int sk, int h, int d) {
 attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v, void *o,
                                      float *lse, int b, int sq, int sk, int h, int d, float scale,
                                      int num_splits, attn_dtype_t dtype, cudaStream_t stream) {
-    attn_status_t st = validate(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
     if (static_cast<int64_t>(b) * cdiv(sq, dec_rows_per_cta(sq)) > 65535) return ATTN_ERR_UNSUPPORTED;
@@ -217,7 +232,7 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
     a.blocks_per_split = static_cast<int>(cdiv(nblocks, splits));
     a.scale_log2 = scale * kLog2e;
     a.status = ds->status;
-    a.flags = g_flags;
+    a.flags = debug_flags();
 
     if (splits == 1)
         return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "exattn.h"
+
 namespace exattn {
 
 // ------------------------------------------------------------ forward
@@ -62,5 +64,15 @@ cudaError_t launch_combine(int d, bool bf16, const float *o_part, const float *l
                            float *lse, int b, int sq, int h, int splits, cudaStream_t stream);
 
 constexpr uint32_t kFlagSkipLoads = 1u;
+
+// ------------------------------------------------------------ host helpers (api.cu)
+// None of these allocates device memory.
+bool load_tensor_map_encoder();
+unsigned int debug_flags();
+attn_status_t validate_args(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, int b, int sq, int sk, int h, int d, float scale,
+                            int dtype);
+bool encode_4d(CUtensorMap *map, const void *base, bool bf16, int d, int h, int s, int b,
+               int box0, int box2, CUtensorMapSwizzle swizzle);
 
 }  // namespace exattn

@@ -81,6 +81,43 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
                                      int num_splits, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * Split-KV decode that allocates no device memory. The pages have no
+ * counterpart: this is a library convenience, not part of the method.
+ *
+ * For callers that cannot call cudaMalloc once they are running: an
+ * application whose device memory is all owned by its own allocator or pool,
+ * code under a fixed memory budget, or real-time code that forbids
+ * allocation after start-up. attn_decode_splitkv_ex takes its per-split
+ * partials from the device's memory pool; this entry point keeps them in
+ * one fixed scratch array of ATTN_NOALLOC_SCRATCH_BYTES compiled into the
+ * library instead, and calls no cudaMalloc, cudaFree or other allocating
+ * routine. Every GPU that loads the library holds that array until the
+ * process exits.
+ *
+ * Arguments, layouts and results are those of attn_decode_splitkv_ex; the
+ * caller still passes all inputs and outputs. With more than one split the
+ * partials need 4 * splits * b * sq * h * (d + 1) bytes (each part rounded
+ * up to 256); a request that needs more than the array holds returns
+ * ATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *
+ * The first call on a device does a one-time set-up: it looks up the
+ * array's device address and clears this entry point's status word with
+ * cudaMemset (legacy default stream); make that first call before any
+ * stream capture. All calls share the one
+ * array, which keeps the last call's contents (every split rewrites all of
+ * its partials, so none is read stale): calls that overlap on the GPU, from
+ * different streams or host threads, race on it and must be serialised by
+ * the caller. A bounded-wait timeout in this entry point's kernels is
+ * recorded in its own status word and is not reported by
+ * attn_get_device_status().
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status_t attn_decode_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
+                                          float *lse, int b, int sq, int sk, int h, int d,
+                                          float scale, int num_splits, attn_dtype_t dtype,
+                                          cudaStream_t stream);
+
+/*
  * The split heuristic for num_splits = 0 on the current device (same issue:
  * split only when the b * h * ceil(sq / rows per CTA) work units leave SMs
  * idle). Returns the split count (>= 1), or 0 on invalid sizes or when no

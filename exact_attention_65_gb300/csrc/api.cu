@@ -153,6 +153,8 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        cudaStream_t stream) {
     attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
+    // work units (256 query rows of one batch and head) must fit an int
+    if (cdiv(sq, FWD_BM * FWD_QTILES) * h * b > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     const bool bf16 = dtype == ATTN_BF16;
@@ -172,6 +174,7 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     a.scale_log2 = scale * kLog2e;
     a.status = ds->status;
     a.flags = debug_flags();
+    a.num_sms = ds->num_sms;
     return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -214,6 +214,10 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
         if (lane == 0) mbar_arrive(empty(s));
     }
 
+    // The reduce grid may begin launching now; it waits for this grid to
+    // complete before it reads any partial.
+    griddep_launch_dependents();
+
     // ---------------------------------------- merge the lane-group states
     // All consumers are past their last read of the ring before it is reused,
     // and all of them agree on whether the split was abandoned.
@@ -372,11 +376,20 @@ __global__ void __launch_bounds__(128)
     const int64_t o_stride = rows * D;
     constexpr float kLog2e = 1.4426950408889634f;
 
+    // The partials come from the split kernel, which may still be draining
+    // when this grid starts (programmatic dependent launch).
+    griddep_wait();
+
+    // Lane i holds LSE_i of the splits i, i+32, ... Every load below is
+    // independent of the ones before it, so the warp keeps many in flight
+    // instead of paying one memory latency per split.
     float mx = -INFINITY;
+#pragma unroll 4
     for (int i = lane; i < splits; i += 32) mx = fmaxf(mx, lse_part[i * lse_stride + lse_idx]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float tot = 0.f;
+#pragma unroll 4
     for (int i = lane; i < splits; i += 32) {
         const float li = lse_part[i * lse_stride + lse_idx];
         tot += (li == -INFINITY) ? 0.f : fast_exp2((li - mx) * kLog2e);
@@ -389,14 +402,19 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     const bool active = D >= 32 || lane < D;
-    for (int i = 0; i < splits; ++i) {
-        const float li = lse_part[i * lse_stride + lse_idx];
-        if (li == -INFINITY) continue;  // empty split: weight 0
-        const float w = fast_exp2((li - L) * kLog2e);
-        const float *src = o_part + i * o_stride + r * D;
-        if (active) {
+    const float *src = o_part + r * D + (active ? lane : 0);
+    for (int i0 = 0; i0 < splits; i0 += 32) {
+        // weight of split i0 + lane (0 for an empty split or past the end)
+        const float li = (i0 + lane < splits) ? lse_part[(i0 + lane) * lse_stride + lse_idx]
+                                              : -INFINITY;
+        const float wl = (li == -INFINITY) ? 0.f : fast_exp2((li - L) * kLog2e);
+        const int n = min(32, splits - i0);
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, src[lane + 32 * e], acc[e]);
+            for (int e = 0; e < PER; ++e)
+                acc[e] = fmaf(w, src[(i0 + j) * o_stride + 32 * e], acc[e]);
         }
     }
     if (active) {
@@ -438,9 +456,20 @@ template <int D, bool BF16>
 cudaError_t launch_combine_t(const float *o_part, const float *lse_part, void *o, float *lse, int b,
                              int sq, int h, int splits, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(b) * sq * h;
-    const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
-    combine_kernel<D, BF16><<<blocks, 128, 0, stream>>>(o_part, lse_part, o, lse, b, sq, h, splits);
-    return cudaGetLastError();
+    // Programmatic dependent launch: this grid is set up while the split
+    // grid drains; griddep_wait() inside orders the memory accesses.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, BF16>, o_part, lse_part, o, lse, b, sq, h,
+                              splits);
 }
 
 }  // namespace

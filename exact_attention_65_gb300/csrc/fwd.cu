@@ -9,21 +9,32 @@
 // partial output rescaled whenever the reference max moves (section 3.3).
 // The per-row log-sum-exp is emitted beside O.
 //
-// CTA layout (384 threads, one CTA per SM):
-//   warp 0        TMA producer: Q tiles once, then K_j and V_j through a
-//                 ring of STAGES slots each.
+// Persistent CTAs (one per SM, 384 threads) loop over work units; a unit is
+// two 128-row query tiles of one (batch, head), and the units are visited
+// query block first, so CTAs running at the same time share the head's K/V
+// through L2. Roles:
+//   warp 0        TMA producer: the unit's Q tiles, then K_j and V_j through
+//                 a ring of STAGES slots each; it runs ahead into the next
+//                 unit as soon as the slots free up.
 //   warp 1        TMEM owner and MMA issuer (one thread): S_j(t) = Q_t K_j^T
 //                 into TMEM, then O_t += P_j(t) V_j with P read from TMEM.
-//   warps 2-3     idle (kept so the softmax warps start at a warpgroup
-//                 boundary, which the TMEM lane quarters require).
-//   warps 4-7     softmax for query tile 0, warps 8-11 for query tile 1:
-//                 thread i owns row i of its tile (TMEM lane i).
+//   warps 2-3     idle.
+//   warps 4-7     softmax and epilogue for query tile 0, warps 8-11 for
+//                 query tile 1: thread i of warp w owns row 32 (w % 4) + i of
+//                 its tile (a warp may only touch its quarter of TMEM lanes).
+// Registers are rebalanced per warpgroup with setmaxnreg: warps 0-3 drop to
+// 80 per thread and the two softmax warpgroups rise to 208, within the
+// 384 x 168 the CTA is launched with.
 // The two query tiles ping-pong: while one warpgroup exponentiates its S
-// tile, the tensor core works on the other tile's MMAs.
+// tile, the tensor core works on the other tile's MMAs. A warpgroup hands
+// its O accumulator back (o_empty) once it has read it out, so the next
+// unit's QK^T MMAs overlap this unit's epilogue.
 //
 // TMEM (512 columns, fp32): tile t uses columns [256t, 256t+128) for S_j,
 // overwritten in place by P_j packed two 16-bit values per column, and
-// [256t+128, 256t+128+d) for the O accumulator.
+// [256t+128, 256t+128+d) for the O accumulator. tcgen05.mma instructions
+// issued by one thread execute in order, so S_{j+1}(t) is only written after
+// P_j(t) V_j has read P_j(t) from the same columns.
 //
 // Lazy rescaling: a row keeps its reference max m until a tile's max
 // exceeds it by more than 8 (log2 units). P = 2^(s*c - m) then stays at most
@@ -57,23 +68,25 @@ struct FwdGeom {
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_TILE_STRIDE = 256;
     static constexpr int TMEM_O_OFF = 128;
-    static constexpr int OCH = D < 32 ? D : 32;  // O columns per TMEM load in the epilogue
+    static constexpr int OCH = D < 32 ? D : 32;  // O columns per TMEM access
 
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + QT * Q_TILE_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * KV_TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE_BYTES;
-    // barriers: q | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] | s_full[QT] | p_full[QT] |
-    //           o_full[QT] | done
-    static constexpr int BAR_Q = 0;
-    static constexpr int BAR_KF = 1;
+    // barriers: q_full | q_empty | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] |
+    //           s_full[QT] | p_full[QT] | o_full[QT] | o_empty[QT] | done
+    static constexpr int BAR_QF = 0;
+    static constexpr int BAR_QE = 1;
+    static constexpr int BAR_KF = 2;
     static constexpr int BAR_KE = BAR_KF + STAGES;
     static constexpr int BAR_VF = BAR_KE + STAGES;
     static constexpr int BAR_VE = BAR_VF + STAGES;
     static constexpr int BAR_SF = BAR_VE + STAGES;
     static constexpr int BAR_PF = BAR_SF + QT;
     static constexpr int BAR_OF = BAR_PF + QT;
-    static constexpr int BAR_DONE = BAR_OF + QT;
+    static constexpr int BAR_OE = BAR_OF + QT;
+    static constexpr int BAR_DONE = BAR_OE + QT;
     static constexpr int NUM_BARS = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int USED = OFF_MISC + 16;
@@ -83,6 +96,14 @@ struct FwdGeom {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(D % 16 == 0 && D >= 16 && D <= 128, "head dim");
 };
+
+// Per-thread register budgets after the rebalance: 4 warps at kRegsControl
+// plus 8 at kRegsSoftmax may not exceed 12 warps at the launch's 168.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 80;
+constexpr int kRegsSoftmax = 208;
+static_assert(4 * kRegsControl + 8 * kRegsSoftmax <= 12 * kRegsLaunch, "register split");
+static_assert(FWD_THREADS == 12 * 32, "three warpgroups");
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -95,78 +116,128 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// A work unit: query rows [m0, m0 + 256) of one (batch, head); n_qt of its
+// two 128-row tiles hold rows below sq.
+struct Unit {
+    int m0, head, batch, n_qt;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int nqb, const FwdArgs &a) {
+    Unit x;
+    const int qb = u % nqb;
+    const int r = u / nqb;
+    x.head = r % a.h;
+    x.batch = r / a.h;
+    x.m0 = qb * (FWD_BM * FWD_QTILES);
+    x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
+    return x;
+}
+
 template <int D>
 __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
-                                             const CUtensorMap *tv, uint32_t sbase, int head,
-                                             int batch, int m0, int n_qt, int nkv,
+                                             const CUtensorMap *tv, uint32_t sbase, int nqb,
+                                             int units, int nkv, const FwdArgs &a,
                                              const WaitGuard &g) {
     using G = FwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     const uint64_t keep = policy_evict_last();  // K/V are re-read by every query block of the head
 
-    mbar_arrive_expect_tx(bar(G::BAR_Q), n_qt * G::Q_TILE_BYTES);
-    for (int t = 0; t < n_qt; ++t)
-        for (int p = 0; p < G::PANELS; ++p)
-            tma_load_4d(sbase + G::OFF_Q + t * G::Q_TILE_BYTES + p * G::Q_PANEL_BYTES, tq,
-                        bar(G::BAR_Q), p * G::PANEL_ELEMS, head, m0 + t * G::BM, batch);
-
-    int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < nkv; ++j) {
-        const int s = j % G::STAGES;
-        const uint32_t ph = (j / G::STAGES) & 1;
-        if (!mbar_wait(bar(G::BAR_KE + s), ph ^ 1, g, 1)) break;
-        mbar_arrive_expect_tx(bar(G::BAR_KF + s), G::KV_TILE_BYTES);
-        for (int p = 0; p < G::PANELS; ++p)
-            tma_load_4d_hint(sbase + G::OFF_K + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES, tk,
-                             bar(G::BAR_KF + s), p * G::PANEL_ELEMS, head, j * G::BN, batch, keep);
-        ++k_issued;
-        if (!mbar_wait(bar(G::BAR_VE + s), ph ^ 1, g, 2)) break;
-        mbar_arrive_expect_tx(bar(G::BAR_VF + s), G::KV_TILE_BYTES);
-        for (int p = 0; p < G::PANELS; ++p)
-            tma_load_4d_hint(sbase + G::OFF_V + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES, tv,
-                             bar(G::BAR_VF + s), p * G::PANEL_ELEMS, head, j * G::BN, batch, keep);
-        ++v_issued;
+    int q_issued = 0, k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const Unit x = unit_of(u, nqb, a);
+        // The Q slot is free once every S MMA of the previous unit has completed.
+        if (!mbar_wait(bar(G::BAR_QE), (q_issued & 1) ^ 1, g, 1)) break;
+        mbar_arrive_expect_tx(bar(G::BAR_QF), x.n_qt * G::Q_TILE_BYTES);
+        for (int t = 0; t < x.n_qt; ++t)
+            for (int p = 0; p < G::PANELS; ++p)
+                tma_load_4d(sbase + G::OFF_Q + t * G::Q_TILE_BYTES + p * G::Q_PANEL_BYTES, tq,
+                            bar(G::BAR_QF), p * G::PANEL_ELEMS, x.head, x.m0 + t * G::BM, x.batch);
+        ++q_issued;
+        for (int j = 0; j < nkv; ++j) {
+            const int s = k_issued % G::STAGES;
+            const uint32_t ph = (k_issued / G::STAGES) & 1;
+            if (!mbar_wait(bar(G::BAR_KE + s), ph ^ 1, g, 2)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(bar(G::BAR_KF + s), G::KV_TILE_BYTES);
+            for (int p = 0; p < G::PANELS; ++p)
+                tma_load_4d_hint(sbase + G::OFF_K + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
+                                 tk, bar(G::BAR_KF + s), p * G::PANEL_ELEMS, x.head, j * G::BN,
+                                 x.batch, keep);
+            ++k_issued;
+            if (!mbar_wait(bar(G::BAR_VE + s), ph ^ 1, g, 3)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(bar(G::BAR_VF + s), G::KV_TILE_BYTES);
+            for (int p = 0; p < G::PANELS; ++p)
+                tma_load_4d_hint(sbase + G::OFF_V + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
+                                 tv, bar(G::BAR_VF + s), p * G::PANEL_ELEMS, x.head, j * G::BN,
+                                 x.batch, keep);
+            ++v_issued;
+        }
     }
     // Never leave the CTA with a copy still landing in shared memory: wait
     // (bounded, even after an abort) for the last load issued into each slot.
     WaitGuard drain = g;
     uint32_t no_abort = 0;
     drain.abort = &no_abort;
-    mbar_wait(bar(G::BAR_Q), 0, drain, 9);
-    for (int j = (k_issued > G::STAGES ? k_issued - G::STAGES : 0); j < k_issued; ++j)
-        mbar_wait(bar(G::BAR_KF + j % G::STAGES), (j / G::STAGES) & 1, drain, 10);
-    for (int j = (v_issued > G::STAGES ? v_issued - G::STAGES : 0); j < v_issued; ++j)
-        mbar_wait(bar(G::BAR_VF + j % G::STAGES), (j / G::STAGES) & 1, drain, 11);
+    if (q_issued > 0) mbar_wait(bar(G::BAR_QF), (q_issued - 1) & 1, drain, 9);
+    for (int i = (k_issued > G::STAGES ? k_issued - G::STAGES : 0); i < k_issued; ++i)
+        mbar_wait(bar(G::BAR_KF + i % G::STAGES), (i / G::STAGES) & 1, drain, 10);
+    for (int i = (v_issued > G::STAGES ? v_issued - G::STAGES : 0); i < v_issued; ++i)
+        mbar_wait(bar(G::BAR_VF + i % G::STAGES), (i / G::STAGES) & 1, drain, 11);
 }
 
 template <int D, bool BF16>
-__device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int n_qt, int nkv,
-                                        const WaitGuard &g) {
+__device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, int units,
+                                        int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     constexpr uint32_t idesc_s = mma_idesc_f16(G::BM, G::BN, BF16, false, false);
     constexpr uint32_t idesc_o = mma_idesc_f16(G::BM, D, BF16, false, true);
 
-    if (mbar_wait(bar(G::BAR_Q), 0, g, 3)) {
-        for (int j = 0; j <= nkv; ++j) {
-            if (j < nkv && !mbar_wait(bar(G::BAR_KF + j % G::STAGES), (j / G::STAGES) & 1, g, 4))
+    int it_u = 0;     // units processed by this CTA
+    int kv_base = 0;  // K/V tiles consumed before the current unit
+    int p_cnt[G::QT] = {};  // P phases consumed per query tile
+    int o_cnt[G::QT] = {};  // units finished per query tile
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
+        const Unit x = unit_of(u, nqb, a);
+        if (!mbar_wait(bar(G::BAR_QF), it_u & 1, g, 4)) break;
+        for (int j = 0; ok && j <= nkv; ++j) {
+            const int cur = kv_base + j, prev = cur - 1;
+            if (j < nkv &&
+                !mbar_wait(bar(G::BAR_KF + cur % G::STAGES), (cur / G::STAGES) & 1, g, 5)) {
+                ok = false;
                 break;
+            }
             if (j > 0 &&
-                !mbar_wait(bar(G::BAR_VF + (j - 1) % G::STAGES), ((j - 1) / G::STAGES) & 1, g, 5))
+                !mbar_wait(bar(G::BAR_VF + prev % G::STAGES), (prev / G::STAGES) & 1, g, 6)) {
+                ok = false;
                 break;
+            }
             tc_fence_after();
-            bool ok = true;
-            for (int t = 0; t < n_qt; ++t) {
+            for (int t = 0; t < x.n_qt; ++t) {
                 const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE;
                 const uint32_t tO = tS + G::TMEM_O_OFF;
                 if (j > 0) {
-                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8 columns.
-                    if (!mbar_wait(bar(G::BAR_PF + t), (j - 1) & 1, g, 6)) {
+                    // The first P V of a unit overwrites O_t: the previous unit's
+                    // epilogue must have read it out.
+                    if (j == 1 && !mbar_wait(bar(G::BAR_OE + t), (o_cnt[t] & 1) ^ 1, g, 7)) {
                         ok = false;
                         break;
                     }
+                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8 columns.
+                    if (!mbar_wait(bar(G::BAR_PF + t), p_cnt[t] & 1, g, 8)) {
+                        ok = false;
+                        break;
+                    }
+                    ++p_cnt[t];
                     tc_fence_after();
-                    const uint32_t vb = sbase + G::OFF_V + ((j - 1) % G::STAGES) * G::KV_TILE_BYTES;
+                    const uint32_t vb = sbase + G::OFF_V + (prev % G::STAGES) * G::KV_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < G::BN / 16; ++kk) {
                         const uint64_t bdesc = smem_desc(vb + kk * 16 * G::ROW_BYTES,
@@ -177,7 +248,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int n_qt,
                 if (j < nkv) {
                     // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
                     const uint32_t qb = sbase + G::OFF_Q + t * G::Q_TILE_BYTES;
-                    const uint32_t kb = sbase + G::OFF_K + (j % G::STAGES) * G::KV_TILE_BYTES;
+                    const uint32_t kb = sbase + G::OFF_K + (cur % G::STAGES) * G::KV_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int p = (kk * 16) / G::PANEL_ELEMS;
@@ -194,9 +265,12 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int n_qt,
                 }
             }
             if (!ok) break;
-            if (j > 0) mma_commit(bar(G::BAR_VE + (j - 1) % G::STAGES));
-            if (j < nkv) mma_commit(bar(G::BAR_KE + j % G::STAGES));
+            if (j == nkv - 1) mma_commit(bar(G::BAR_QE));  // last read of this unit's Q
+            if (j > 0) mma_commit(bar(G::BAR_VE + prev % G::STAGES));
+            if (j < nkv) mma_commit(bar(G::BAR_KE + cur % G::STAGES));
         }
+        kv_base += nkv;
+        for (int t = 0; t < x.n_qt; ++t) ++o_cnt[t];
     }
     // No MMA may still be running when TMEM is released.
     mma_commit(bar(G::BAR_DONE));
@@ -207,149 +281,177 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int n_qt,
 }
 
 template <int D, bool BF16>
-__device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4,
-                                            int head, int batch, int m0, int nkv, const FwdArgs &a,
+__device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4, int nqb,
+                                            int units, int nkv, const FwdArgs &a,
                                             const WaitGuard &g) {
     using G = FwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     const uint32_t lane = threadIdx.x & 31;
     const int row = q4 * 32 + lane;
-    const int grow = m0 + t * G::BM + row;
     const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE + (static_cast<uint32_t>(q4 * 32) << 16);
     const uint32_t tO = tS + G::TMEM_O_OFF;
     const float c = a.scale_log2;
     const bool c_pos = c >= 0.f;
+    int s_cnt = 0, o_cnt = 0;
 
-    float m_ref = -INFINITY;  // reference max, log2 units
-    float l = 0.f;            // running sum of 2^(s*c - m_ref)
-    bool alive = true;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit x = unit_of(u, nqb, a);
+        if (t >= x.n_qt) continue;
+        const int tile_row0 = x.m0 + t * G::BM;
+        const int grow = tile_row0 + row;
+        // A warp whose 32 rows all lie past sq skips the math but keeps the
+        // barrier protocol.
+        const bool warp_live = tile_row0 + q4 * 32 < a.sq;
 
-    for (int j = 0; j < nkv; ++j) {
-        bool ok = mbar_wait(bar(G::BAR_SF + t), j & 1, g, 7);
-        if (!__all_sync(0xffffffffu, ok)) {
-            alive = false;
-            break;
+        float m_ref = -INFINITY;  // reference max, log2 units
+        float l = 0.f;            // running sum of 2^(s*c - m_ref)
+        bool alive = true;
+        for (int j = 0; j < nkv; ++j) {
+            const bool ok = mbar_wait(bar(G::BAR_SF + t), s_cnt & 1, g, 13);
+            ++s_cnt;
+            if (!__all_sync(0xffffffffu, ok)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            if (warp_live) {
+                const int valid = a.sk - j * G::BN;  // keys of this tile inside [0, sk)
+                const bool ragged = valid < G::BN;
+                uint32_t sr[G::BN];
+#pragma unroll
+                for (int c0 = 0; c0 < G::BN; c0 += 32) {
+                    if (!ragged || c0 < valid)
+                        tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+                }
+                tmem_wait_ld();
+                const float *s = reinterpret_cast<const float *>(sr);
+
+                // row max of the scaled scores (min of the raw ones if scale < 0)
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
+                if (!ragged) {
+                    if (c_pos) {
+#pragma unroll
+                        for (int i = 0; i < G::BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < G::BN; ++i) mx[i & 7] = fminf(mx[i & 7], s[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < G::BN; ++i) {
+                        if (i < valid)
+                            mx[i & 7] = c_pos ? fmaxf(mx[i & 7], s[i]) : fminf(mx[i & 7], s[i]);
+                    }
+                }
+                float mraw = mx[0];
+#pragma unroll
+                for (int i = 1; i < 8; ++i) mraw = c_pos ? fmaxf(mraw, mx[i]) : fminf(mraw, mx[i]);
+                const float m_tile = mraw * c;
+
+                const bool need = m_tile > m_ref + 8.0f;
+                const float m_new = need ? m_tile : m_ref;
+                const float alpha = fast_exp2(m_ref - m_new);  // 1 if kept, 0 on the first tile
+                m_ref = m_new;
+
+                // P = 2^(s*c - m_ref), packed in pairs into the S columns; keys
+                // past sk get exactly 0 (their V rows are TMA zero fill).
+                const float neg_m = -m_ref;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[G::BN / 2];
+#pragma unroll
+                for (int i = 0; i < G::BN / 2; ++i) {
+                    float x0 = fmaf(s[2 * i], c, neg_m);
+                    float x1 = fmaf(s[2 * i + 1], c, neg_m);
+                    if (ragged) {
+                        x0 = (2 * i < valid) ? x0 : -INFINITY;
+                        x1 = (2 * i + 1 < valid) ? x1 : -INFINITY;
+                    }
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    ls[i & 3] += p0 + p1;
+                    pk[i] = pack2<BF16>(p0, p1);
+                }
+                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+#pragma unroll
+                for (int c0 = 0; c0 < G::BN / 2; c0 += 32)
+                    tmem_st32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&pk[c0]));
+
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O row *= alpha; P_{j-1} V_{j-1} has completed (S_j's commit covers it).
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += G::OCH) {
+                        if constexpr (G::OCH == 32) {
+                            uint32_t ov[32];
+                            tmem_ld32(tO + c0, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                            tmem_st32(tO + c0, ov);
+                        } else {
+                            uint32_t ov[16];
+                            tmem_ld16(tO + c0, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                            tmem_st16(tO + c0, ov);
+                        }
+                    }
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
         }
+        if (!alive) return;
+
+        // ---------------------------------------------------- epilogue
+        const bool ok = mbar_wait(bar(G::BAR_OF + t), o_cnt & 1, g, 14);
+        ++o_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
-        uint32_t sr[G::BN];
-#pragma unroll
-        for (int c0 = 0; c0 < G::BN; c0 += 32)
-            tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
-        tmem_wait_ld();
-        float *s = reinterpret_cast<float *>(sr);
-
-        const int valid = a.sk - j * G::BN;  // keys of this tile inside [0, sk)
-        const bool ragged = valid < G::BN;
-
-        // row max of the scaled scores (min of the raw ones if scale < 0)
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
-        if (!ragged) {
-            if (c_pos) {
-#pragma unroll
-                for (int i = 0; i < G::BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < G::BN; ++i) mx[i & 7] = fminf(mx[i & 7], s[i]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < G::BN; ++i) {
-                if (i < valid) mx[i & 7] = c_pos ? fmaxf(mx[i & 7], s[i]) : fminf(mx[i & 7], s[i]);
-            }
-        }
-        float mraw = mx[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) mraw = c_pos ? fmaxf(mraw, mx[i]) : fminf(mraw, mx[i]);
-        const float m_tile = mraw * c;
-
-        const bool need = m_tile > m_ref + 8.0f;
-        const float m_new = need ? m_tile : m_ref;
-        const float alpha = fast_exp2(m_ref - m_new);  // 1 if kept, 0 on the first tile
-        m_ref = m_new;
-
-        // P = 2^(s*c - m_ref), packed in pairs into the S columns.
-        const float neg_m = -m_ref;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[G::BN / 2];
-#pragma unroll
-        for (int i = 0; i < G::BN / 2; ++i) {
-            float p0 = fast_exp2(fmaf(s[2 * i], c, neg_m));
-            float p1 = fast_exp2(fmaf(s[2 * i + 1], c, neg_m));
-            if (ragged) {
-                p0 = (2 * i < valid) ? p0 : 0.f;
-                p1 = (2 * i + 1 < valid) ? p1 : 0.f;
-            }
-            ls[i & 3] += p0 + p1;
-            pk[i] = pack2<BF16>(p0, p1);
-        }
-        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-#pragma unroll
-        for (int c0 = 0; c0 < G::BN / 2; c0 += 32)
-            tmem_st32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&pk[c0]));
-
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // O row *= alpha; PV_{j-1} has completed (S_j's commit covers it).
+        // Read O_t a chunk at a time, normalise, pack to 16 bits and store;
+        // then hand the accumulator back to the MMA issuer.
+        const float inv_l = 1.0f / l;
+        const bool row_out = warp_live && grow < a.sq;
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            reinterpret_cast<uint16_t *>(a.o) +
+            ((static_cast<int64_t>(x.batch) * a.sq + (row_out ? grow : 0)) * a.h + x.head) * D);
+        if (warp_live) {
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += G::OCH) {
-                if constexpr (G::OCH == 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + c0, ov);
-                    tmem_wait_ld();
+                uint32_t ov[G::OCH];
+                if constexpr (G::OCH == 32)
+                    tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(ov));
+                else
+                    tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
+                tmem_wait_ld();
+                if (row_out) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(tO + c0, ov);
-                } else {
-                    uint32_t ov[16];
-                    tmem_ld16(tO + c0, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st16(tO + c0, ov);
+                    for (int i = 0; i < G::OCH / 8; ++i)
+                        dst[c0 / 8 + i] = make_uint4(
+                            pack2<BF16>(__uint_as_float(ov[8 * i]) * inv_l,
+                                        __uint_as_float(ov[8 * i + 1]) * inv_l),
+                            pack2<BF16>(__uint_as_float(ov[8 * i + 2]) * inv_l,
+                                        __uint_as_float(ov[8 * i + 3]) * inv_l),
+                            pack2<BF16>(__uint_as_float(ov[8 * i + 4]) * inv_l,
+                                        __uint_as_float(ov[8 * i + 5]) * inv_l),
+                            pack2<BF16>(__uint_as_float(ov[8 * i + 6]) * inv_l,
+                                        __uint_as_float(ov[8 * i + 7]) * inv_l));
                 }
             }
         }
-        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
+        if (lane == 0) mbar_arrive(bar(G::BAR_OE + t));
+        if (row_out)
+            a.lse[(static_cast<int64_t>(x.batch) * a.h + x.head) * a.sq + grow] =
+                (m_ref + __log2f(l)) * 0.69314718055994530942f;
     }
-
-    if (!alive) return;
-    bool ok = mbar_wait(bar(G::BAR_OF + t), 0, g, 8);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-
-    const float inv_l = 1.0f / l;
-    const bool in_range = grow < a.sq;
-    using Elem = uint16_t;
-    Elem *orow = reinterpret_cast<Elem *>(a.o) +
-                 ((static_cast<int64_t>(batch) * a.sq + grow) * a.h + head) * D;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += G::OCH) {
-        uint32_t ov[G::OCH];
-        if constexpr (G::OCH == 32)
-            tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(ov));
-        else
-            tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
-        tmem_wait_ld();
-        uint32_t packed[G::OCH / 2];
-#pragma unroll
-        for (int i = 0; i < G::OCH / 2; ++i)
-            packed[i] = pack2<BF16>(__uint_as_float(ov[2 * i]) * inv_l,
-                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
-        if (in_range) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
-#pragma unroll
-            for (int i = 0; i < G::OCH / 8; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
-        }
-    }
-    if (in_range)
-        a.lse[(static_cast<int64_t>(batch) * a.h + head) * a.sq + grow] =
-            (m_ref + __log2f(l)) * 0.69314718055994530942f;
 }
 
 template <int D, bool BF16>
@@ -365,9 +467,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
-    const int head = blockIdx.y, batch = blockIdx.z;
-    const int m0 = blockIdx.x * (G::BM * G::QT);
-    const int n_qt = min(G::QT, (a.sq - m0 + G::BM - 1) / G::BM);
+    const int nqb = (a.sq + G::BM * G::QT - 1) / (G::BM * G::QT);
+    const int units = nqb * a.h * a.b;
     const int nkv = (a.sk + G::BN - 1) / G::BN;
 
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + G::OFF_MISC);
@@ -376,7 +477,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i) {
             uint32_t count = 1;
-            if (i >= G::BAR_PF && i < G::BAR_PF + G::QT) count = 4;  // one arrive per softmax warp
+            // one arrive per softmax warp
+            if ((i >= G::BAR_PF && i < G::BAR_PF + G::QT) || (i >= G::BAR_OE && i < G::BAR_OE + G::QT))
+                count = 4;
             mbar_init(bar(i), count);
         }
         *abort_flag = 0u;
@@ -397,14 +500,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitGuard g{abort_flag, a.status, kKernFwd};
 
-    if (warp == 0) {
-        if (lane == 0 && !(a.flags & kFlagSkipLoads))
-            fwd_producer<D>(&tq, &tk, &tv, sbase, head, batch, m0, n_qt, nkv, g);
-    } else if (warp == 1) {
-        if (lane == 0) fwd_mma<D, BF16>(sbase, tmem, n_qt, nkv, g);
-    } else if (warp >= 4) {
-        const int t = (warp - 4) >> 2;
-        if (t < n_qt) fwd_softmax<D, BF16>(sbase, tmem, t, warp & 3, head, batch, m0, nkv, a, g);
+    if (warp < 4) {
+        reg_dealloc<kRegsControl>();
+        if (warp == 0) {
+            if (lane == 0 && !(a.flags & kFlagSkipLoads))
+                fwd_producer<D>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+        } else if (warp == 1) {
+            if (lane == 0) fwd_mma<D, BF16>(sbase, tmem, nqb, units, nkv, a, g);
+        }
+    } else {
+        reg_alloc<kRegsSoftmax>();
+        fwd_softmax<D, BF16>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv, a, g);
     }
 
     tc_fence_before();
@@ -427,8 +533,11 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid((a.sq + G::BM * G::QT - 1) / (G::BM * G::QT), a.h, a.b);
-    fwd_kernel<D, BF16><<<grid, FWD_THREADS, G::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+    const int64_t nqb = (a.sq + G::BM * G::QT - 1) / (G::BM * G::QT);
+    const int64_t units = nqb * a.h * a.b;
+    const int64_t ctas = units < a.num_sms ? units : a.num_sms;
+    fwd_kernel<D, BF16><<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(
+        tq, tk, tv, a);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@ struct FwdArgs {
     float scale_log2;  // scale * log2(e)
     uint32_t *status;
     uint32_t flags;
+    int num_sms;  // persistent grid: at most one CTA per SM
 };
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,

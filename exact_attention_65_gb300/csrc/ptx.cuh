@@ -77,9 +77,11 @@ struct WaitGuard {
 
 // Waits until the mbarrier phase with the given parity has completed.
 // Returns false (and records the site) if the bound ran out or another
-// thread of the CTA already gave up.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitGuard &g,
-                                            uint32_t site) {
+// thread of the CTA already gave up. Inlined: a call from a region whose
+// register budget was changed with setmaxnreg would need one budget for all
+// callers.
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                      const WaitGuard &g, uint32_t site) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < kWaitMaxPolls; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -283,6 +285,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---------------------------------------------------------------- register rebalancing
+// Executed by every thread of a warpgroup (4 consecutive, aligned warps).
+// The increases of all warpgroups may not exceed what the decreases release
+// from the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Blocks until the grid this one depends on has completed and its memory
+// is visible (returns at once when launched without such a dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the dependent grid begin launching before this grid has finished.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace exattn

@@ -37,7 +37,7 @@ def _worker(rank, world, port, out):
 def test_two_rank_aggregation_takes_max_time_and_total_work():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         results = dict(out)

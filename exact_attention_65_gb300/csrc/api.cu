@@ -184,9 +184,11 @@ int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_
     const int64_t units = static_cast<int64_t>(b) * h * cdiv(sq, dec_rows_per_cta(sq));
     const int64_t nblocks = cdiv(sk, dec_block_rows(d));
     if (units >= num_sms) return 1;  // every SM already has work: no reason to split
-    // Otherwise aim at two CTAs per SM (two decode CTAs fit in one SM's
-    // shared memory), without making splits smaller than one key block.
-    int64_t s = cdiv(2 * static_cast<int64_t>(num_sms), units);
+    // Otherwise give each SM one CTA: one CTA keeps three 32 KB K/V blocks
+    // requested ahead, which is enough bytes in flight per SM, and more CTAs
+    // than SMs would leave a second, partial wave on some SMs. Splits are
+    // never smaller than one key block.
+    int64_t s = static_cast<int64_t>(num_sms) / units;
     if (s > nblocks) s = nblocks;
     if (s > 128) s = 128;
     return s < 1 ? 1 : static_cast<int>(s);

@@ -89,15 +89,19 @@ def test_heuristic_follows_the_parallel_work_rule(exattn_lib):
     # issue, and a GB300's SM count).
     for sms in (108, 132, 148, 152):
         assert f(8, 1, 8192, 48, 128, sms) == 1
-    # b=1, h=16, sq=1: 16 units leave SMs idle, so split; about two CTAs per SM.
-    s = f(1, 1, 32768, 16, 128, 148)
-    assert s == -(-2 * 148 // 16)
-    assert 16 * s >= 148
+    # b=1, h=16, sq=1: 16 units leave SMs idle, so split; as many CTAs as fit
+    # one per SM.
+    for sms in (148, 152):
+        s = f(1, 1, 32768, 16, 128, sms)
+        assert s == sms // 16
+        assert 16 * s <= sms < 16 * (s + 1)
     # never more splits than key blocks (64 rows of d=128 per block)
     assert f(1, 1, 100, 1, 128, 148) == 2
     assert f(1, 1, 1, 1, 128, 148) == 1
     # sq > 1: units count query blocks of 4 rows
-    assert f(2, 10, 65536, 8, 128, 148) == -(-2 * 148 // (2 * 8 * 3))
+    assert f(2, 10, 65536, 8, 128, 148) == 148 // (2 * 8 * 3)
+    # 100 units: two splits would need 200 CTAs, more than the SMs, so one
+    assert f(1, 1, 65536, 100, 128, 148) == 1
     # more work units than SMs at any sq
     assert f(64, 16, 4096, 32, 64, 148) == 1
     # invalid sizes

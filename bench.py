@@ -457,6 +457,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-problem extra timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--profile-only", choices=sorted(workloads.WORKLOADS), default=None,
+                    help="profiling aid: only run warmup + steps calls of one workload's kernels "
+                         "(no timing, no JSON line), e.g. under ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -464,10 +467,32 @@ def main(argv=None):
     if args.gpus != ws and not (args.gpus == 1 and ws == 1):
         if ws == 1 and args.gpus > 1:
             ap.error("--gpus N > 1 runs under torchrun, one process per GPU")
-    if args.impl == "reference":
+    if args.profile_only:
+        run_profile_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
+
+
+def run_profile_only(args):
+    """Runs one workload's kernels (forward, or split-KV decode with the
+    heuristic split count) warmup + steps times on seeded device inputs."""
+    import exact_attention_65_gb300 as ea
+
+    w = workloads.WORKLOADS[args.profile_only]
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(workloads.SEED)
+    q = torch.randn((w.b, w.sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+    k = torch.randn((w.b, w.sk, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+    v = torch.randn((w.b, w.sk, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+    fn = (lambda: ea.attn_fwd(q, k, v)) if w.kind == "fwd" else (
+        lambda: ea.attn_decode_splitkv(q, k, v, num_splits=0))
+    for _ in range(args.warmup + args.steps):
+        fn()
+    if ea.attn_get_device_status() != ea.ATTN_OK:
+        raise RuntimeError("a kernel reported a timeout")
 
 
 if __name__ == "__main__":

@@ -14,7 +14,7 @@
 // query block first, so CTAs running at the same time share the head's K/V
 // through L2. Roles:
 //   warp 0        TMA producer: the unit's Q tiles, then K_j and V_j through
-//                 a ring of STAGES slots each; it runs ahead into the next
+//                 one ring of K/V slots; it runs ahead into the next
 //                 unit as soon as the slots free up.
 //   warp 1        TMEM owner and MMA issuer (one thread): S_j(t) = Q_t K_j^T
 //                 into TMEM, then O_t += P_j(t) V_j with P read from TMEM.
@@ -61,7 +61,8 @@ struct FwdGeom {
     static constexpr int KV_PANEL_BYTES = BN * ROW_BYTES;
     static constexpr int Q_TILE_BYTES = BM * D * 2;
     static constexpr int KV_TILE_BYTES = BN * D * 2;
-    static constexpr int STAGES = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    // One ring of K/V tile slots; items flow K_0, V_0, K_1, V_1, ...
+    static constexpr int SLOTS = D == 128 ? 5 : 8;
     static constexpr uint32_t LAYOUT =
         ROW_BYTES == 128 ? kLayoutSw128 : (ROW_BYTES == 64 ? kLayoutSw64 : kLayoutSw32);
     static constexpr uint32_t SBO = 8 * ROW_BYTES;  // bytes between 8-row core-matrix groups
@@ -71,20 +72,17 @@ struct FwdGeom {
     static constexpr int OCH = D < 32 ? D : 32;  // O columns per TMEM access
 
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + QT * Q_TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE_BYTES;
-    // barriers: q_full | q_empty | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] |
-    //           s_full[QT] | p_full[QT] | o_full[QT] | o_empty[QT] | done
+    static constexpr int OFF_KV = OFF_Q + QT * Q_TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_KV + SLOTS * KV_TILE_BYTES;
+    // barriers: q_full | q_empty | kv_full[SLOTS] | kv_empty[SLOTS] |
+    //           s_full[QT] | p_full[2 QT] | o_full[QT] | o_empty[QT] | done
     static constexpr int BAR_QF = 0;
     static constexpr int BAR_QE = 1;
-    static constexpr int BAR_KF = 2;
-    static constexpr int BAR_KE = BAR_KF + STAGES;
-    static constexpr int BAR_VF = BAR_KE + STAGES;
-    static constexpr int BAR_VE = BAR_VF + STAGES;
-    static constexpr int BAR_SF = BAR_VE + STAGES;
-    static constexpr int BAR_PF = BAR_SF + QT;
-    static constexpr int BAR_OF = BAR_PF + QT;
+    static constexpr int BAR_KVF = 2;
+    static constexpr int BAR_KVE = BAR_KVF + SLOTS;
+    static constexpr int BAR_SF = BAR_KVE + SLOTS;
+    static constexpr int BAR_PF = BAR_SF + QT;      // two per tile: P keys 0-63, 64-127
+    static constexpr int BAR_OF = BAR_PF + 2 * QT;
     static constexpr int BAR_OE = BAR_OF + QT;
     static constexpr int BAR_DONE = BAR_OE + QT;
     static constexpr int NUM_BARS = BAR_DONE + 1;
@@ -107,13 +105,10 @@ static_assert(FWD_THREADS == 12 * 32, "three warpgroups");
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if constexpr (BF16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&v);
-    }
+    if constexpr (BF16)
+        return cvt_pack_bf16(lo, hi);
+    else
+        return cvt_pack_f16(lo, hi);
 }
 
 // A work unit: query rows [m0, m0 + 256) of one (batch, head); n_qt of its
@@ -142,7 +137,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     const uint64_t keep = policy_evict_last();  // K/V are re-read by every query block of the head
 
-    int q_issued = 0, k_issued = 0, v_issued = 0;
+    int q_issued = 0, n_issued = 0;  // n counts ring items (K and V tiles)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Unit x = unit_of(u, nqb, a);
@@ -154,29 +149,20 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
                 tma_load_4d(sbase + G::OFF_Q + t * G::Q_TILE_BYTES + p * G::Q_PANEL_BYTES, tq,
                             bar(G::BAR_QF), p * G::PANEL_ELEMS, x.head, x.m0 + t * G::BM, x.batch);
         ++q_issued;
-        for (int j = 0; j < nkv; ++j) {
-            const int s = k_issued % G::STAGES;
-            const uint32_t ph = (k_issued / G::STAGES) & 1;
-            if (!mbar_wait(bar(G::BAR_KE + s), ph ^ 1, g, 2)) {
+        for (int i = 0; i < 2 * nkv; ++i) {  // K_j at i = 2j, V_j at i = 2j + 1
+            const int s = n_issued % G::SLOTS;
+            const uint32_t ph = (n_issued / G::SLOTS) & 1;
+            if (!mbar_wait(bar(G::BAR_KVE + s), ph ^ 1, g, 2)) {
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(bar(G::BAR_KF + s), G::KV_TILE_BYTES);
+            mbar_arrive_expect_tx(bar(G::BAR_KVF + s), G::KV_TILE_BYTES);
+            const CUtensorMap *map = (i & 1) ? tv : tk;
             for (int p = 0; p < G::PANELS; ++p)
-                tma_load_4d_hint(sbase + G::OFF_K + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
-                                 tk, bar(G::BAR_KF + s), p * G::PANEL_ELEMS, x.head, j * G::BN,
-                                 x.batch, keep);
-            ++k_issued;
-            if (!mbar_wait(bar(G::BAR_VE + s), ph ^ 1, g, 3)) {
-                ok = false;
-                break;
-            }
-            mbar_arrive_expect_tx(bar(G::BAR_VF + s), G::KV_TILE_BYTES);
-            for (int p = 0; p < G::PANELS; ++p)
-                tma_load_4d_hint(sbase + G::OFF_V + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
-                                 tv, bar(G::BAR_VF + s), p * G::PANEL_ELEMS, x.head, j * G::BN,
-                                 x.batch, keep);
-            ++v_issued;
+                tma_load_4d_hint(sbase + G::OFF_KV + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
+                                 map, bar(G::BAR_KVF + s), p * G::PANEL_ELEMS, x.head,
+                                 (i >> 1) * G::BN, x.batch, keep);
+            ++n_issued;
         }
     }
     // Never leave the CTA with a copy still landing in shared memory: wait
@@ -185,10 +171,8 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     uint32_t no_abort = 0;
     drain.abort = &no_abort;
     if (q_issued > 0) mbar_wait(bar(G::BAR_QF), (q_issued - 1) & 1, drain, 9);
-    for (int i = (k_issued > G::STAGES ? k_issued - G::STAGES : 0); i < k_issued; ++i)
-        mbar_wait(bar(G::BAR_KF + i % G::STAGES), (i / G::STAGES) & 1, drain, 10);
-    for (int i = (v_issued > G::STAGES ? v_issued - G::STAGES : 0); i < v_issued; ++i)
-        mbar_wait(bar(G::BAR_VF + i % G::STAGES), (i / G::STAGES) & 1, drain, 11);
+    for (int n = (n_issued > G::SLOTS ? n_issued - G::SLOTS : 0); n < n_issued; ++n)
+        mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
 }
 
 template <int D, bool BF16>
@@ -208,14 +192,14 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
         const Unit x = unit_of(u, nqb, a);
         if (!mbar_wait(bar(G::BAR_QF), it_u & 1, g, 4)) break;
         for (int j = 0; ok && j <= nkv; ++j) {
-            const int cur = kv_base + j, prev = cur - 1;
-            if (j < nkv &&
-                !mbar_wait(bar(G::BAR_KF + cur % G::STAGES), (cur / G::STAGES) & 1, g, 5)) {
+            // ring items: K_j is item 2 (kv_base + j), V_{j-1} the item before it
+            const int nk = 2 * (kv_base + j), nv = nk - 1;
+            const int ks = nk % G::SLOTS, vs = nv % G::SLOTS;
+            if (j < nkv && !mbar_wait(bar(G::BAR_KVF + ks), (nk / G::SLOTS) & 1, g, 5)) {
                 ok = false;
                 break;
             }
-            if (j > 0 &&
-                !mbar_wait(bar(G::BAR_VF + prev % G::STAGES), (prev / G::STAGES) & 1, g, 6)) {
+            if (j > 0 && !mbar_wait(bar(G::BAR_KVF + vs), (nv / G::SLOTS) & 1, g, 6)) {
                 ok = false;
                 break;
             }
@@ -230,25 +214,30 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                         ok = false;
                         break;
                     }
-                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8 columns.
-                    if (!mbar_wait(bar(G::BAR_PF + t), p_cnt[t] & 1, g, 8)) {
-                        ok = false;
-                        break;
-                    }
-                    ++p_cnt[t];
-                    tc_fence_after();
-                    const uint32_t vb = sbase + G::OFF_V + (prev % G::STAGES) * G::KV_TILE_BYTES;
+                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8
+                    // columns. The softmax hands P over in two halves of 64 keys, so
+                    // the first half's MMAs start while the second is still computed.
+                    const uint32_t vb = sbase + G::OFF_KV + vs * G::KV_TILE_BYTES;
+                    for (int half = 0; half < 2; ++half) {
+                        if (!mbar_wait(bar(G::BAR_PF + 2 * t + half), p_cnt[t] & 1, g, 8)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < G::BN / 16; ++kk) {
-                        const uint64_t bdesc = smem_desc(vb + kk * 16 * G::ROW_BYTES,
-                                                         G::KV_PANEL_BYTES, G::SBO, G::LAYOUT);
-                        mma_ts(tO, tS + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                        for (int kk = half * G::BN / 32; kk < (half + 1) * G::BN / 32; ++kk) {
+                            const uint64_t bdesc = smem_desc(vb + kk * 16 * G::ROW_BYTES,
+                                                             G::KV_PANEL_BYTES, G::SBO, G::LAYOUT);
+                            mma_ts(tO, tS + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                        }
                     }
+                    if (!ok) break;
+                    ++p_cnt[t];
                 }
                 if (j < nkv) {
                     // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
                     const uint32_t qb = sbase + G::OFF_Q + t * G::Q_TILE_BYTES;
-                    const uint32_t kb = sbase + G::OFF_K + (cur % G::STAGES) * G::KV_TILE_BYTES;
+                    const uint32_t kb = sbase + G::OFF_KV + ks * G::KV_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int p = (kk * 16) / G::PANEL_ELEMS;
@@ -266,8 +255,8 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
             }
             if (!ok) break;
             if (j == nkv - 1) mma_commit(bar(G::BAR_QE));  // last read of this unit's Q
-            if (j > 0) mma_commit(bar(G::BAR_VE + prev % G::STAGES));
-            if (j < nkv) mma_commit(bar(G::BAR_KE + cur % G::STAGES));
+            if (j > 0) mma_commit(bar(G::BAR_KVE + vs));
+            if (j < nkv) mma_commit(bar(G::BAR_KVE + ks));
         }
         kv_base += nkv;
         for (int t = 0; t < x.n_qt; ++t) ++o_cnt[t];
@@ -327,27 +316,28 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 const float *s = reinterpret_cast<const float *>(sr);
 
                 // row max of the scaled scores (min of the raw ones if scale < 0)
-                float mx[8];
+                float mx[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
+                for (int i = 0; i < 4; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
                 if (!ragged) {
                     if (c_pos) {
 #pragma unroll
-                        for (int i = 0; i < G::BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                        for (int i = 0; i < G::BN / 2; ++i)
+                            mx[i & 3] = max3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < G::BN; ++i) mx[i & 7] = fminf(mx[i & 7], s[i]);
+                        for (int i = 0; i < G::BN / 2; ++i)
+                            mx[i & 3] = min3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < G::BN; ++i) {
                         if (i < valid)
-                            mx[i & 7] = c_pos ? fmaxf(mx[i & 7], s[i]) : fminf(mx[i & 7], s[i]);
+                            mx[i & 3] = c_pos ? fmaxf(mx[i & 3], s[i]) : fminf(mx[i & 3], s[i]);
                     }
                 }
-                float mraw = mx[0];
-#pragma unroll
-                for (int i = 1; i < 8; ++i) mraw = c_pos ? fmaxf(mraw, mx[i]) : fminf(mraw, mx[i]);
+                const float mraw = c_pos ? fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3])
+                                         : fminf(min3f(mx[0], mx[1], mx[2]), mx[3]);
                 const float m_tile = mraw * c;
 
                 const bool need = m_tile > m_ref + 8.0f;
@@ -355,57 +345,78 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 const float alpha = fast_exp2(m_ref - m_new);  // 1 if kept, 0 on the first tile
                 m_ref = m_new;
 
-                // P = 2^(s*c - m_ref), packed in pairs into the S columns; keys
-                // past sk get exactly 0 (their V rows are TMA zero fill).
-                const float neg_m = -m_ref;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[G::BN / 2];
-#pragma unroll
-                for (int i = 0; i < G::BN / 2; ++i) {
-                    float x0 = fmaf(s[2 * i], c, neg_m);
-                    float x1 = fmaf(s[2 * i + 1], c, neg_m);
-                    if (ragged) {
-                        x0 = (2 * i < valid) ? x0 : -INFINITY;
-                        x1 = (2 * i + 1 < valid) ? x1 : -INFINITY;
-                    }
-                    const float p0 = fast_exp2(x0);
-                    const float p1 = fast_exp2(x1);
-                    ls[i & 3] += p0 + p1;
-                    pk[i] = pack2<BF16>(p0, p1);
-                }
-                l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-#pragma unroll
-                for (int c0 = 0; c0 < G::BN / 2; c0 += 32)
-                    tmem_st32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&pk[c0]));
+                // O must be rescaled (rare once the running max settles) before
+                // the MMA issuer accumulates P_j V_j into it. The rescale runs
+                // after both halves of P are stored, when the scores are no longer
+                // held in registers; in such a step the first half is handed over
+                // only after it.
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
 
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O row *= alpha; P_{j-1} V_{j-1} has completed (S_j's commit covers it).
+                // P = 2^(s*c - m_ref), packed in pairs into the S columns and
+                // handed to the MMA issuer in two halves of 64 keys; keys past sk
+                // get exactly 0 (their V rows are TMA zero fill).
+                const float neg_m = -m_ref;
+                const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
+                uint64_t acc2[2] = {0ull, 0ull};  // packed partial row sums (0.0f bits)
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += G::OCH) {
-                        if constexpr (G::OCH == 32) {
-                            uint32_t ov[32];
-                            tmem_ld32(tO + c0, ov);
-                            tmem_wait_ld();
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[G::BN / 4];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                            tmem_st32(tO + c0, ov);
-                        } else {
-                            uint32_t ov[16];
-                            tmem_ld16(tO + c0, ov);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                            tmem_st16(tO + c0, ov);
+                    for (int i = 0; i < G::BN / 4; ++i) {
+                        const int k0 = half * (G::BN / 2) + 2 * i;
+                        float x0, x1;
+                        // x = s * c - m for two keys in one packed FMA
+                        f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
+                        if (ragged) {
+                            x0 = (k0 < valid) ? x0 : -INFINITY;
+                            x1 = (k0 + 1 < valid) ? x1 : -INFINITY;
                         }
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
+                        pk[i] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st32(tS + half * (G::BN / 4), pk);
+                    if (half == 0 && !rescale) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(G::BAR_PF + 2 * t));
+                    }
+                }
+                if (rescale) {
+                    // O row *= alpha; P_{j-1} V_{j-1} has completed (S_j's commit
+                    // covers it). 16 columns at a time keeps this path spill-free.
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        uint32_t ov[16];
+                        tmem_ld16(tO + c0, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st16(tO + c0, ov);
                     }
                 }
                 tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (rescale) mbar_arrive(bar(G::BAR_PF + 2 * t));
+                    mbar_arrive(bar(G::BAR_PF + 2 * t + 1));
+                }
+                float a0, a1, a2, a3;
+                f2_split(acc2[0], a0, a1);
+                f2_split(acc2[1], a2, a3);
+                l = l * alpha + ((a0 + a1) + (a2 + a3));
+            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(G::BAR_PF + 2 * t));
+                    mbar_arrive(bar(G::BAR_PF + 2 * t + 1));
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
         }
         if (!alive) return;
 
@@ -478,7 +489,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         for (int i = 0; i < G::NUM_BARS; ++i) {
             uint32_t count = 1;
             // one arrive per softmax warp
-            if ((i >= G::BAR_PF && i < G::BAR_PF + G::QT) || (i >= G::BAR_OE && i < G::BAR_OE + G::QT))
+            if ((i >= G::BAR_PF && i < G::BAR_PF + 2 * G::QT) ||
+                (i >= G::BAR_OE && i < G::BAR_OE + G::QT))
                 count = 4;
             mbar_init(bar(i), count);
         }

@@ -182,6 +182,14 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     constexpr uint32_t idesc_s = mma_idesc_f16(G::BM, G::BN, BF16, false, false);
     constexpr uint32_t idesc_o = mma_idesc_f16(G::BM, D, BF16, false, true);
+    // This one thread issues every MMA of the CTA and is on the critical path,
+    // so descriptors are built once here: the start-address field is the low
+    // 14 bits of (address >> 4), so an offset of x bytes within shared memory
+    // is added as x >> 4 without touching the other fields.
+    const uint64_t dq = smem_desc(sbase + G::OFF_Q, 16, G::SBO, G::LAYOUT);    // Q, K-major
+    const uint64_t dk = smem_desc(sbase + G::OFF_KV, 16, G::SBO, G::LAYOUT);   // K, K-major
+    const uint64_t dv =
+        smem_desc(sbase + G::OFF_KV, G::KV_PANEL_BYTES, G::SBO, G::LAYOUT);  // V, MN-major
 
     int it_u = 0;     // units processed by this CTA
     int kv_base = 0;  // K/V tiles consumed before the current unit
@@ -217,7 +225,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                     // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8
                     // columns. The softmax hands P over in two halves of 64 keys, so
                     // the first half's MMAs start while the second is still computed.
-                    const uint32_t vb = sbase + G::OFF_KV + vs * G::KV_TILE_BYTES;
+                    const uint64_t vdesc = dv + ((vs * G::KV_TILE_BYTES) >> 4);
                     for (int half = 0; half < 2; ++half) {
                         if (!mbar_wait(bar(G::BAR_PF + 2 * t + half), p_cnt[t] & 1, g, 8)) {
                             ok = false;
@@ -225,28 +233,24 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                         }
                         tc_fence_after();
 #pragma unroll
-                        for (int kk = half * G::BN / 32; kk < (half + 1) * G::BN / 32; ++kk) {
-                            const uint64_t bdesc = smem_desc(vb + kk * 16 * G::ROW_BYTES,
-                                                             G::KV_PANEL_BYTES, G::SBO, G::LAYOUT);
-                            mma_ts(tO, tS + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = half * G::BN / 32; kk < (half + 1) * G::BN / 32; ++kk)
+                            mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * G::ROW_BYTES) >> 4),
+                                   idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
                     }
                     if (!ok) break;
                     ++p_cnt[t];
                 }
                 if (j < nkv) {
                     // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
-                    const uint32_t qb = sbase + G::OFF_Q + t * G::Q_TILE_BYTES;
-                    const uint32_t kb = sbase + G::OFF_KV + ks * G::KV_TILE_BYTES;
+                    const uint64_t qdesc = dq + ((t * G::Q_TILE_BYTES) >> 4);
+                    const uint64_t kdesc = dk + ((ks * G::KV_TILE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int p = (kk * 16) / G::PANEL_ELEMS;
                         const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
-                        const uint64_t adesc =
-                            smem_desc(qb + p * G::Q_PANEL_BYTES + off, 16, G::SBO, G::LAYOUT);
-                        const uint64_t bdesc =
-                            smem_desc(kb + p * G::KV_PANEL_BYTES + off, 16, G::SBO, G::LAYOUT);
-                        mma_ss(tS, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss(tS, qdesc + ((p * G::Q_PANEL_BYTES + off) >> 4),
+                               kdesc + ((p * G::KV_PANEL_BYTES + off) >> 4), idesc_s,
+                               kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(G::BAR_SF + t));
                 } else {

@@ -75,14 +75,14 @@ struct FwdGeom {
     static constexpr int OFF_KV = OFF_Q + QT * Q_TILE_BYTES;
     static constexpr int OFF_BAR = OFF_KV + SLOTS * KV_TILE_BYTES;
     // barriers: q_full | q_empty | kv_full[SLOTS] | kv_empty[SLOTS] |
-    //           s_full[QT] | p_full[2 QT] | o_full[QT] | o_empty[QT] | done
+    //           s_full[QT] | p_full[QT] | o_full[QT] | o_empty[QT] | done
     static constexpr int BAR_QF = 0;
     static constexpr int BAR_QE = 1;
     static constexpr int BAR_KVF = 2;
     static constexpr int BAR_KVE = BAR_KVF + SLOTS;
     static constexpr int BAR_SF = BAR_KVE + SLOTS;
-    static constexpr int BAR_PF = BAR_SF + QT;      // two per tile: P keys 0-63, 64-127
-    static constexpr int BAR_OF = BAR_PF + 2 * QT;
+    static constexpr int BAR_PF = BAR_SF + QT;
+    static constexpr int BAR_OF = BAR_PF + QT;
     static constexpr int BAR_OE = BAR_OF + QT;
     static constexpr int BAR_DONE = BAR_OE + QT;
     static constexpr int NUM_BARS = BAR_DONE + 1;
@@ -199,19 +199,13 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
         const Unit x = unit_of(u, nqb, a);
         if (!mbar_wait(bar(G::BAR_QF), it_u & 1, g, 4)) break;
+        // The issue order keeps the tensor core's short instruction queue fed:
+        // every barrier wait or commit sits right after a group of MMAs, while
+        // those are still queued, never in a clump between two groups.
         for (int j = 0; ok && j <= nkv; ++j) {
             // ring items: K_j is item 2 (kv_base + j), V_{j-1} the item before it
             const int nk = 2 * (kv_base + j), nv = nk - 1;
             const int ks = nk % G::SLOTS, vs = nv % G::SLOTS;
-            if (j < nkv && !mbar_wait(bar(G::BAR_KVF + ks), (nk / G::SLOTS) & 1, g, 5)) {
-                ok = false;
-                break;
-            }
-            if (j > 0 && !mbar_wait(bar(G::BAR_KVF + vs), (nv / G::SLOTS) & 1, g, 6)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
             for (int t = 0; t < x.n_qt; ++t) {
                 const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE;
                 const uint32_t tO = tS + G::TMEM_O_OFF;
@@ -222,25 +216,28 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                         ok = false;
                         break;
                     }
-                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys per 8
-                    // columns. The softmax hands P over in two halves of 64 keys, so
-                    // the first half's MMAs start while the second is still computed.
-                    const uint64_t vdesc = dv + ((vs * G::KV_TILE_BYTES) >> 4);
-                    for (int half = 0; half < 2; ++half) {
-                        if (!mbar_wait(bar(G::BAR_PF + 2 * t + half), p_cnt[t] & 1, g, 8)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = half * G::BN / 32; kk < (half + 1) * G::BN / 32; ++kk)
-                            mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * G::ROW_BYTES) >> 4),
-                                   idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                    // O_t += P_{j-1}(t) V_{j-1}; P sits in the S columns, 16 keys
+                    // per 8 columns. V_{j-1} was waited for at the end of step j-1.
+                    if (!mbar_wait(bar(G::BAR_PF + t), p_cnt[t] & 1, g, 8)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
                     ++p_cnt[t];
+                    tc_fence_after();
+                    const uint64_t vdesc = dv + ((vs * G::KV_TILE_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < G::BN / 16; ++kk)
+                        mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_o,
+                               (j > 1 || kk > 0) ? 1u : 0u);
+                    if (t == x.n_qt - 1) mma_commit(bar(G::BAR_KVE + vs));  // last read of V_{j-1}
                 }
                 if (j < nkv) {
+                    if (t == 0 &&
+                        !mbar_wait(bar(G::BAR_KVF + ks), (nk / G::SLOTS) & 1, g, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
                     const uint64_t qdesc = dq + ((t * G::Q_TILE_BYTES) >> 4);
                     const uint64_t kdesc = dk + ((ks * G::KV_TILE_BYTES) >> 4);
@@ -253,14 +250,21 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                                kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(G::BAR_SF + t));
+                    if (t == x.n_qt - 1) {
+                        mma_commit(bar(G::BAR_KVE + ks));                  // last read of K_j
+                        if (j == nkv - 1) mma_commit(bar(G::BAR_QE));  // ... and of this Q
+                    }
                 } else {
                     mma_commit(bar(G::BAR_OF + t));
                 }
             }
             if (!ok) break;
-            if (j == nkv - 1) mma_commit(bar(G::BAR_QE));  // last read of this unit's Q
-            if (j > 0) mma_commit(bar(G::BAR_KVE + vs));
-            if (j < nkv) mma_commit(bar(G::BAR_KVE + ks));
+            // V_j for the next step, waited for while the S MMAs above are queued
+            if (j < nkv &&
+                !mbar_wait(bar(G::BAR_KVF + (nk + 1) % G::SLOTS), ((nk + 1) / G::SLOTS) & 1, g, 6)) {
+                ok = false;
+                break;
+            }
         }
         kv_base += nkv;
         for (int t = 0; t < x.n_qt; ++t) ++o_cnt[t];
@@ -351,14 +355,13 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
 
                 // O must be rescaled (rare once the running max settles) before
                 // the MMA issuer accumulates P_j V_j into it. The rescale runs
-                // after both halves of P are stored, when the scores are no longer
-                // held in registers; in such a step the first half is handed over
-                // only after it.
+                // after P is stored, when the scores are no longer held in
+                // registers, and before P is handed over.
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
 
-                // P = 2^(s*c - m_ref), packed in pairs into the S columns and
-                // handed to the MMA issuer in two halves of 64 keys; keys past sk
-                // get exactly 0 (their V rows are TMA zero fill).
+                // P = 2^(s*c - m_ref), packed in pairs into the S columns, 64 keys
+                // at a time; keys past sk get exactly 0 (their V rows are TMA
+                // zero fill).
                 const float neg_m = -m_ref;
                 const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
                 uint64_t acc2[2] = {0ull, 0ull};  // packed partial row sums (0.0f bits)
@@ -381,12 +384,6 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                         pk[i] = pack2<BF16>(p0, p1);
                     }
                     tmem_st32(tS + half * (G::BN / 4), pk);
-                    if (half == 0 && !rescale) {
-                        tmem_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(G::BAR_PF + 2 * t));
-                    }
                 }
                 if (rescale) {
                     // O row *= alpha; P_{j-1} V_{j-1} has completed (S_j's commit
@@ -405,10 +402,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if (rescale) mbar_arrive(bar(G::BAR_PF + 2 * t));
-                    mbar_arrive(bar(G::BAR_PF + 2 * t + 1));
-                }
+                if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
                 float a0, a1, a2, a3;
                 f2_split(acc2[0], a0, a1);
                 f2_split(acc2[1], a2, a3);
@@ -416,10 +410,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
             } else {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(G::BAR_PF + 2 * t));
-                    mbar_arrive(bar(G::BAR_PF + 2 * t + 1));
-                }
+                if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
             }
         }
         if (!alive) return;
@@ -493,7 +484,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         for (int i = 0; i < G::NUM_BARS; ++i) {
             uint32_t count = 1;
             // one arrive per softmax warp
-            if ((i >= G::BAR_PF && i < G::BAR_PF + 2 * G::QT) ||
+            if ((i >= G::BAR_PF && i < G::BAR_PF + G::QT) ||
                 (i >= G::BAR_OE && i < G::BAR_OE + G::QT))
                 count = 4;
             mbar_init(bar(i), count);

@@ -63,6 +63,10 @@ struct FwdGeom {
     static constexpr int KV_TILE_BYTES = BN * D * 2;
     // One ring of K/V tile slots; items flow K_0, V_0, K_1, V_1, ...
     static constexpr int SLOTS = D == 128 ? 5 : 8;
+    // Q buffers (QT tiles each). Measured: one Q buffer and a deeper K/V ring
+    // beat two Q buffers and a 3-slot ring at d = 128.
+    static constexpr int QBUF = 1;
+    static constexpr int Q_BUF_BYTES = QT * Q_TILE_BYTES;
     static constexpr uint32_t LAYOUT =
         ROW_BYTES == 128 ? kLayoutSw128 : (ROW_BYTES == 64 ? kLayoutSw64 : kLayoutSw32);
     static constexpr uint32_t SBO = 8 * ROW_BYTES;  // bytes between 8-row core-matrix groups
@@ -72,13 +76,13 @@ struct FwdGeom {
     static constexpr int OCH = D < 32 ? D : 32;  // O columns per TMEM access
 
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + QT * Q_TILE_BYTES;
+    static constexpr int OFF_KV = OFF_Q + QBUF * Q_BUF_BYTES;
     static constexpr int OFF_BAR = OFF_KV + SLOTS * KV_TILE_BYTES;
     // barriers: q_full | q_empty | kv_full[SLOTS] | kv_empty[SLOTS] |
     //           s_full[QT] | p_full[QT] | o_full[QT] | o_empty[QT] | done
-    static constexpr int BAR_QF = 0;
-    static constexpr int BAR_QE = 1;
-    static constexpr int BAR_KVF = 2;
+    static constexpr int BAR_QF = 0;            // [QBUF]
+    static constexpr int BAR_QE = BAR_QF + QBUF;  // [QBUF]
+    static constexpr int BAR_KVF = BAR_QE + QBUF;
     static constexpr int BAR_KVE = BAR_KVF + SLOTS;
     static constexpr int BAR_SF = BAR_KVE + SLOTS;
     static constexpr int BAR_PF = BAR_SF + QT;
@@ -141,13 +145,16 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Unit x = unit_of(u, nqb, a);
-        // The Q slot is free once every S MMA of the previous unit has completed.
-        if (!mbar_wait(bar(G::BAR_QE), (q_issued & 1) ^ 1, g, 1)) break;
-        mbar_arrive_expect_tx(bar(G::BAR_QF), x.n_qt * G::Q_TILE_BYTES);
+        // A Q buffer is free once every S MMA of the unit two back has completed.
+        const int qb = q_issued % G::QBUF;
+        if (!mbar_wait(bar(G::BAR_QE + qb), ((q_issued / G::QBUF) & 1) ^ 1, g, 1)) break;
+        mbar_arrive_expect_tx(bar(G::BAR_QF + qb), x.n_qt * G::Q_TILE_BYTES);
         for (int t = 0; t < x.n_qt; ++t)
             for (int p = 0; p < G::PANELS; ++p)
-                tma_load_4d(sbase + G::OFF_Q + t * G::Q_TILE_BYTES + p * G::Q_PANEL_BYTES, tq,
-                            bar(G::BAR_QF), p * G::PANEL_ELEMS, x.head, x.m0 + t * G::BM, x.batch);
+                tma_load_4d(sbase + G::OFF_Q + qb * G::Q_BUF_BYTES + t * G::Q_TILE_BYTES +
+                                p * G::Q_PANEL_BYTES,
+                            tq, bar(G::BAR_QF + qb), p * G::PANEL_ELEMS, x.head, x.m0 + t * G::BM,
+                            x.batch);
         ++q_issued;
         for (int i = 0; i < 2 * nkv; ++i) {  // K_j at i = 2j, V_j at i = 2j + 1
             const int s = n_issued % G::SLOTS;
@@ -170,7 +177,8 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     WaitGuard drain = g;
     uint32_t no_abort = 0;
     drain.abort = &no_abort;
-    if (q_issued > 0) mbar_wait(bar(G::BAR_QF), (q_issued - 1) & 1, drain, 9);
+    for (int n = (q_issued > G::QBUF ? q_issued - G::QBUF : 0); n < q_issued; ++n)
+        mbar_wait(bar(G::BAR_QF + n % G::QBUF), (n / G::QBUF) & 1, drain, 9);
     for (int n = (n_issued > G::SLOTS ? n_issued - G::SLOTS : 0); n < n_issued; ++n)
         mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
 }
@@ -198,7 +206,8 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
         const Unit x = unit_of(u, nqb, a);
-        if (!mbar_wait(bar(G::BAR_QF), it_u & 1, g, 4)) break;
+        const int qbuf = it_u % G::QBUF;
+        if (!mbar_wait(bar(G::BAR_QF + qbuf), (it_u / G::QBUF) & 1, g, 4)) break;
         // The issue order keeps the tensor core's short instruction queue fed:
         // every barrier wait or commit sits right after a group of MMAs, while
         // those are still queued, never in a clump between two groups.
@@ -239,7 +248,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                     }
                     tc_fence_after();
                     // S_j(t) = Q_t K_j^T, 16 head-dim elements per instruction.
-                    const uint64_t qdesc = dq + ((t * G::Q_TILE_BYTES) >> 4);
+                    const uint64_t qdesc = dq + ((qbuf * G::Q_BUF_BYTES + t * G::Q_TILE_BYTES) >> 4);
                     const uint64_t kdesc = dk + ((ks * G::KV_TILE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -252,7 +261,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                     mma_commit(bar(G::BAR_SF + t));
                     if (t == x.n_qt - 1) {
                         mma_commit(bar(G::BAR_KVE + ks));                  // last read of K_j
-                        if (j == nkv - 1) mma_commit(bar(G::BAR_QE));  // ... and of this Q
+                        if (j == nkv - 1) mma_commit(bar(G::BAR_QE + qbuf));  // ... and of this Q
                     }
                 } else {
                     mma_commit(bar(G::BAR_OF + t));
@@ -368,20 +377,32 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[G::BN / 4];
+                    if (!ragged) {
 #pragma unroll
-                    for (int i = 0; i < G::BN / 4; ++i) {
-                        const int k0 = half * (G::BN / 2) + 2 * i;
-                        float x0, x1;
-                        // x = s * c - m for two keys in one packed FMA
-                        f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
-                        if (ragged) {
+                        for (int i = 0; i < G::BN / 4; ++i) {
+                            const int k0 = half * (G::BN / 2) + 2 * i;
+                            float x0, x1;
+                            // x = s * c - m for two keys in one packed FMA
+                            f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
+                            const float p0 = fast_exp2(x0);
+                            const float p1 = fast_exp2(x1);
+                            acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
+                            pk[i] = pack2<BF16>(p0, p1);
+                        }
+                    } else {
+                        // last key tile: keys past sk are masked to exactly 0
+#pragma unroll
+                        for (int i = 0; i < G::BN / 4; ++i) {
+                            const int k0 = half * (G::BN / 2) + 2 * i;
+                            float x0, x1;
+                            f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
                             x0 = (k0 < valid) ? x0 : -INFINITY;
                             x1 = (k0 + 1 < valid) ? x1 : -INFINITY;
+                            const float p0 = fast_exp2(x0);
+                            const float p1 = fast_exp2(x1);
+                            acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
+                            pk[i] = pack2<BF16>(p0, p1);
                         }
-                        const float p0 = fast_exp2(x0);
-                        const float p1 = fast_exp2(x1);
-                        acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
-                        pk[i] = pack2<BF16>(p0, p1);
                     }
                     tmem_st32(tS + half * (G::BN / 4), pk);
                 }

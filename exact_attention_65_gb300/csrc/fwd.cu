@@ -23,7 +23,7 @@
 //                 query tile 1: thread i of warp w owns row 32 (w % 4) + i of
 //                 its tile (a warp may only touch its quarter of TMEM lanes).
 // Registers are rebalanced per warpgroup with setmaxnreg: warps 0-3 drop to
-// 80 per thread and the two softmax warpgroups rise to 208, within the
+// 96 per thread and the two softmax warpgroups rise to 200, within the
 // 384 x 168 the CTA is launched with.
 // The two query tiles ping-pong: while one warpgroup exponentiates its S
 // tile, the tensor core works on the other tile's MMAs. A warpgroup hands
@@ -102,8 +102,8 @@ struct FwdGeom {
 // Per-thread register budgets after the rebalance: 4 warps at kRegsControl
 // plus 8 at kRegsSoftmax may not exceed 12 warps at the launch's 168.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsControl = 80;
-constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 96;  // below this the MMA issuer spills
+constexpr int kRegsSoftmax = 200;
 static_assert(4 * kRegsControl + 8 * kRegsSoftmax <= 12 * kRegsLaunch, "register split");
 static_assert(FWD_THREADS == 12 * 32, "three warpgroups");
 
@@ -444,6 +444,9 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         // Read O_t a chunk at a time, normalise, pack to 16 bits and store;
         // then hand the accumulator back to the MMA issuer.
         const float inv_l = 1.0f / l;
+        // Rows start at multiples of 2d bytes (>= 32); only the base of O may
+        // be merely 16-byte aligned.
+        const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
         const bool row_out = warp_live && grow < a.sq;
         uint4 *dst = reinterpret_cast<uint4 *>(
             reinterpret_cast<uint16_t *>(a.o) +
@@ -458,17 +461,23 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                     tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
                 tmem_wait_ld();
                 if (row_out) {
+                    uint32_t pk[G::OCH / 2];
 #pragma unroll
-                    for (int i = 0; i < G::OCH / 8; ++i)
-                        dst[c0 / 8 + i] = make_uint4(
-                            pack2<BF16>(__uint_as_float(ov[8 * i]) * inv_l,
-                                        __uint_as_float(ov[8 * i + 1]) * inv_l),
-                            pack2<BF16>(__uint_as_float(ov[8 * i + 2]) * inv_l,
-                                        __uint_as_float(ov[8 * i + 3]) * inv_l),
-                            pack2<BF16>(__uint_as_float(ov[8 * i + 4]) * inv_l,
-                                        __uint_as_float(ov[8 * i + 5]) * inv_l),
-                            pack2<BF16>(__uint_as_float(ov[8 * i + 6]) * inv_l,
-                                        __uint_as_float(ov[8 * i + 7]) * inv_l));
+                    for (int i = 0; i < G::OCH / 2; ++i)
+                        pk[i] = pack2<BF16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                            __uint_as_float(ov[2 * i + 1]) * inv_l);
+                    if (o_al32) {
+                        // whole 32-byte sectors: 16 columns per store
+#pragma unroll
+                        for (int i = 0; i < G::OCH / 16; ++i)
+                            st_global_v8(dst + c0 / 8 + 2 * i,
+                                         *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < G::OCH / 8; ++i)
+                            dst[c0 / 8 + i] =
+                                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
         }

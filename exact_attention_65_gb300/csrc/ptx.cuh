@@ -324,6 +324,14 @@ __device__ __forceinline__ uint32_t cvt_pack_f16(float lo, float hi) {
     return r;
 }
 
+// 32-byte global store of eight 32-bit words (sm_100 and later); the address
+// must be 32-byte aligned. A whole sector per thread and instruction.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&r)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // Three-input max / min (one instruction on sm_100 and later).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;

@@ -146,3 +146,22 @@ def test_runs_on_a_side_stream(gpu, oracle_mod):
     s.synchronize()
     o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / 8)
     compare(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_output_only_16_byte_aligned(gpu, oracle_mod, d):
+    """O at an address that is 16- but not 32-byte aligned (the ABI's
+    minimum) takes the 16-byte store path and gives the same result."""
+    b, sq, sk, h = 1, 200, 300, 3
+    q, k, v = workloads.make_qkv(b, sq, sk, h, d, torch.bfloat16, seed=41)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    n = q.numel()
+    buf = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+    base = buf.data_ptr()
+    off = next(e for e in range(16) if (base + 2 * e) % 32 == 16)
+    out = buf[off:off + n].view(q.shape)
+    assert out.data_ptr() % 16 == 0 and out.data_ptr() % 32 != 0
+    o, lse = gpu.attn_fwd(qd, kd, vd, out=out)
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(d))
+    compare(out, lse, o_ref, lse_ref)

@@ -324,29 +324,38 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 const int valid = a.sk - j * G::BN;  // keys of this tile inside [0, sk)
                 const bool ragged = valid < G::BN;
                 uint32_t sr[G::BN];
-#pragma unroll
-                for (int c0 = 0; c0 < G::BN; c0 += 32) {
-                    if (!ragged || c0 < valid)
-                        tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
-                }
-                tmem_wait_ld();
                 const float *s = reinterpret_cast<const float *>(sr);
-
                 // row max of the scaled scores (min of the raw ones if scale < 0)
                 float mx[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
                 if (!ragged) {
-                    if (c_pos) {
+                    // the max of the first 64 scores runs while the rest load
+                    tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_wait_ld();
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
 #pragma unroll
-                        for (int i = 0; i < G::BN / 2; ++i)
-                            mx[i & 3] = max3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
-                    } else {
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1) tmem_wait_ld();
+                        if (c_pos) {
 #pragma unroll
-                        for (int i = 0; i < G::BN / 2; ++i)
-                            mx[i & 3] = min3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
+                            for (int i = part * G::BN / 4; i < (part + 1) * G::BN / 4; ++i)
+                                mx[i & 3] = max3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
+                        } else {
+#pragma unroll
+                            for (int i = part * G::BN / 4; i < (part + 1) * G::BN / 4; ++i)
+                                mx[i & 3] = min3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
+                        }
                     }
                 } else {
+#pragma unroll
+                    for (int c0 = 0; c0 < G::BN; c0 += 32) {
+                        if (c0 < valid)
+                            tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+                    }
+                    tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < G::BN; ++i) {
                         if (i < valid)

@@ -126,7 +126,92 @@ CUtensorMapSwizzle fwd_swizzle(int d) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Per-split partials O_i [splits, b, sq, h, d] then LSE_i [splits, b, h, sq]
+// (fp32), taken stream-ordered from the device's default memory pool.
+attn_status_t alloc_partials(int64_t splits, int b, int sq, int h, int d, cudaStream_t stream,
+                             void **ws, float **o_part, float **lse_part) {
+    const int64_t rows = static_cast<int64_t>(b) * sq * h;
+    const size_t o_bytes = static_cast<size_t>(splits * rows * d) * sizeof(float);
+    const size_t l_bytes = static_cast<size_t>(splits * rows) * sizeof(float);
+    if (cudaMallocAsync(ws, o_bytes + l_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_MEMORY;
+    }
+    *o_part = static_cast<float *>(*ws);
+    *lse_part = reinterpret_cast<float *>(static_cast<char *>(*ws) + o_bytes);
+    return ATTN_OK;
+}
+
+// The tensor-core forward kernel, over all keys (splits = 1) or over key
+// ranges of whole 128-key tiles whose fp32 partials the combine kernel
+// reduces. A split count above the tile count is clamped, and it is lowered
+// so that no split is empty.
+attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b,
+                      int sq, int sk, int h, int d, float scale, bool bf16, int64_t splits,
+                      const DeviceState *ds, cudaStream_t stream) {
+    const int64_t nkv = cdiv(sk, FWD_BN);
+    if (splits > nkv) splits = nkv;
+    if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
+    if (splits < 1) splits = 1;
+    const int64_t tps = cdiv(nkv, splits);
+    splits = cdiv(nkv, tps);
+    // work units (256 query rows of one batch, head and key range) must fit an int
+    const int64_t units = cdiv(sq, FWD_BM * FWD_QTILES) * splits * h * b;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    const int box0 = fwd_row_bytes(d) / 2;
+    CUtensorMap tq, tk, tv;
+    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, FWD_BM, fwd_swizzle(d)) ||
+        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)) ||
+        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)))
+        return ATTN_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.b = b;
+    a.sq = sq;
+    a.sk = sk;
+    a.h = h;
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = debug_flags();
+    a.num_sms = ds->num_sms;
+    a.splits = static_cast<int>(splits);
+    a.tiles_per_split = static_cast<int>(tps);
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    if (splits == 1)
+        return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    void *ws = nullptr;
+    attn_status_t st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, stream);
+    if (e == cudaSuccess)
+        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
+
+namespace exattn {
+
+int dec_num_splits(int b, int sq, int sk, int h, int d, int num_sms) {
+    if (b < 1 || sq < 1 || sk < 1 || h < 1 || num_sms < 1) return 0;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
+    const int64_t units = static_cast<int64_t>(b) * h * cdiv(sq, dec_rows_per_cta(sq));
+    const int64_t nblocks = cdiv(sk, dec_block_rows(d));
+    if (units >= num_sms) return 1;  // every SM already has work: no reason to split
+    // Otherwise give each SM one CTA: one CTA keeps three 32 KB K/V blocks
+    // requested ahead, which is enough bytes in flight per SM, and more CTAs
+    // than SMs would leave a second, partial wave on some SMs. Splits are
+    // never smaller than one key block.
+    int64_t s = static_cast<int64_t>(num_sms) / units;
+    if (s > nblocks) s = nblocks;
+    if (s > 128) s = 128;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+}  // namespace exattn
 
 extern "C" {
 
@@ -153,43 +238,23 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        cudaStream_t stream) {
     attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
-    // work units (256 query rows of one batch and head) must fit an int
-    if (cdiv(sq, FWD_BM * FWD_QTILES) * h * b > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
-    const bool bf16 = dtype == ATTN_BF16;
-    const int box0 = fwd_row_bytes(d) / 2;
-    CUtensorMap tq, tk, tv;
-    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, FWD_BM, fwd_swizzle(d)) ||
-        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)) ||
-        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)))
-        return ATTN_ERR_CUDA;
-    FwdArgs a;
-    a.o = o;
-    a.lse = lse;
-    a.b = b;
-    a.sq = sq;
-    a.sk = sk;
-    a.h = h;
-    a.scale_log2 = scale * kLog2e;
-    a.status = ds->status;
-    a.flags = debug_flags();
-    a.num_sms = ds->num_sms;
-    return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, 1, ds, stream);
 }
 
 int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms) {
+    if (sq == 1) return dec_num_splits(b, sq, sk, h, d, num_sms);
     if (b < 1 || sq < 1 || sk < 1 || h < 1 || num_sms < 1) return 0;
     if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
-    const int64_t units = static_cast<int64_t>(b) * h * cdiv(sq, dec_rows_per_cta(sq));
-    const int64_t nblocks = cdiv(sk, dec_block_rows(d));
-    if (units >= num_sms) return 1;  // every SM already has work: no reason to split
-    // Otherwise give each SM one CTA: one CTA keeps three 32 KB K/V blocks
-    // requested ahead, which is enough bytes in flight per SM, and more CTAs
-    // than SMs would leave a second, partial wave on some SMs. Splits are
-    // never smaller than one key block.
+    // Several query rows: the tensor-core kernel, whose work unit is 256 query
+    // rows of one (batch, head) over a range of 128-key tiles; the same rule,
+    // one CTA per SM.
+    const int64_t units = static_cast<int64_t>(b) * h * cdiv(sq, FWD_BM * FWD_QTILES);
+    const int64_t ntiles = cdiv(sk, FWD_BN);
+    if (units >= num_sms) return 1;
     int64_t s = static_cast<int64_t>(num_sms) / units;
-    if (s > nblocks) s = nblocks;
+    if (s > ntiles) s = ntiles;
     if (s > 128) s = 128;
     return s < 1 ? 1 : static_cast<int>(s);
 }
@@ -206,10 +271,17 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
     attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(b) * cdiv(sq, dec_rows_per_cta(sq)) > 65535) return ATTN_ERR_UNSUPPORTED;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     const bool bf16 = dtype == ATTN_BF16;
+    if (sq > 1) {
+        // Several query rows share every K/V read in the tensor-core kernel,
+        // split along the keys.
+        const int64_t s = num_splits == 0
+                              ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms)
+                              : num_splits;
+        return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, bf16, s, ds, stream);
+    }
     const int64_t nblocks = cdiv(sk, dec_block_rows(d));
     int64_t splits = num_splits == 0
                          ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms)
@@ -242,16 +314,9 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
     if (splits == 1)
         return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 
-    const int64_t rows = static_cast<int64_t>(b) * sq * h;
-    const size_t o_bytes = static_cast<size_t>(splits * rows * d) * sizeof(float);
-    const size_t l_bytes = static_cast<size_t>(splits * rows) * sizeof(float);
     void *ws = nullptr;
-    if (cudaMallocAsync(&ws, o_bytes + l_bytes, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return ATTN_ERR_NO_MEMORY;
-    }
-    a.o_part = static_cast<float *>(ws);
-    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes);
+    if ((st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
+        return st;
     cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
     if (e == cudaSuccess)
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);

@@ -83,7 +83,7 @@ extern "C" attn_status_t attn_decode_splitkv_noalloc(const void *q, const void *
     const bool bf16 = dtype == ATTN_BF16;
     const int64_t nblocks = cdiv(sk, dec_block_rows(d));
     int64_t splits = num_splits == 0
-                         ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, slot->num_sms)
+                         ? dec_num_splits(b, sq, sk, h, d, slot->num_sms)
                          : num_splits;
     if (splits > nblocks) splits = nblocks;
     if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;

@@ -115,20 +115,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         return cvt_pack_f16(lo, hi);
 }
 
-// A work unit: query rows [m0, m0 + 256) of one (batch, head); n_qt of its
+// A work unit: query rows [m0, m0 + 256) of one (batch, head) against key
+// tiles [kv0, kv0 + nkv) (all of them unless the keys are split); n_qt of its
 // two 128-row tiles hold rows below sq.
 struct Unit {
-    int m0, head, batch, n_qt;
+    int m0, head, batch, n_qt, split, kv0, nkv;
 };
 
-__device__ __forceinline__ Unit unit_of(int u, int nqb, const FwdArgs &a) {
+// Units are numbered query block first, then split, head and batch.
+__device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdArgs &a) {
     Unit x;
     const int qb = u % nqb;
-    const int r = u / nqb;
+    int r = u / nqb;
+    x.split = r % a.splits;
+    r /= a.splits;
     x.head = r % a.h;
     x.batch = r / a.h;
     x.m0 = qb * (FWD_BM * FWD_QTILES);
     x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
+    x.kv0 = x.split * a.tiles_per_split;
+    x.nkv = min(a.tiles_per_split, nkv_all - x.kv0);
     return x;
 }
 
@@ -144,7 +150,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     int q_issued = 0, n_issued = 0;  // n counts ring items (K and V tiles)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const Unit x = unit_of(u, nqb, a);
+        const Unit x = unit_of(u, nqb, nkv, a);
         // A Q buffer is free once every S MMA of the unit two back has completed.
         const int qb = q_issued % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QE + qb), ((q_issued / G::QBUF) & 1) ^ 1, g, 1)) break;
@@ -156,7 +162,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
                             tq, bar(G::BAR_QF + qb), p * G::PANEL_ELEMS, x.head, x.m0 + t * G::BM,
                             x.batch);
         ++q_issued;
-        for (int i = 0; i < 2 * nkv; ++i) {  // K_j at i = 2j, V_j at i = 2j + 1
+        for (int i = 0; i < 2 * x.nkv; ++i) {  // K_j at i = 2j, V_j at i = 2j + 1
             const int s = n_issued % G::SLOTS;
             const uint32_t ph = (n_issued / G::SLOTS) & 1;
             if (!mbar_wait(bar(G::BAR_KVE + s), ph ^ 1, g, 2)) {
@@ -168,7 +174,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
             for (int p = 0; p < G::PANELS; ++p)
                 tma_load_4d_hint(sbase + G::OFF_KV + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
                                  map, bar(G::BAR_KVF + s), p * G::PANEL_ELEMS, x.head,
-                                 (i >> 1) * G::BN, x.batch, keep);
+                                 (x.kv0 + (i >> 1)) * G::BN, x.batch, keep);
             ++n_issued;
         }
     }
@@ -205,13 +211,13 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     int o_cnt[G::QT] = {};  // units finished per query tile
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
-        const Unit x = unit_of(u, nqb, a);
+        const Unit x = unit_of(u, nqb, nkv, a);
         const int qbuf = it_u % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QF + qbuf), (it_u / G::QBUF) & 1, g, 4)) break;
         // The issue order keeps the tensor core's short instruction queue fed:
         // every barrier wait or commit sits right after a group of MMAs, while
         // those are still queued, never in a clump between two groups.
-        for (int j = 0; ok && j <= nkv; ++j) {
+        for (int j = 0; ok && j <= x.nkv; ++j) {
             // ring items: K_j is item 2 (kv_base + j), V_{j-1} the item before it
             const int nk = 2 * (kv_base + j), nv = nk - 1;
             const int ks = nk % G::SLOTS, vs = nv % G::SLOTS;
@@ -240,7 +246,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                                (j > 1 || kk > 0) ? 1u : 0u);
                     if (t == x.n_qt - 1) mma_commit(bar(G::BAR_KVE + vs));  // last read of V_{j-1}
                 }
-                if (j < nkv) {
+                if (j < x.nkv) {
                     if (t == 0 &&
                         !mbar_wait(bar(G::BAR_KVF + ks), (nk / G::SLOTS) & 1, g, 5)) {
                         ok = false;
@@ -261,7 +267,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                     mma_commit(bar(G::BAR_SF + t));
                     if (t == x.n_qt - 1) {
                         mma_commit(bar(G::BAR_KVE + ks));                  // last read of K_j
-                        if (j == nkv - 1) mma_commit(bar(G::BAR_QE + qbuf));  // ... and of this Q
+                        if (j == x.nkv - 1) mma_commit(bar(G::BAR_QE + qbuf));  // ... and of this Q
                     }
                 } else {
                     mma_commit(bar(G::BAR_OF + t));
@@ -269,13 +275,13 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
             }
             if (!ok) break;
             // V_j for the next step, waited for while the S MMAs above are queued
-            if (j < nkv &&
+            if (j < x.nkv &&
                 !mbar_wait(bar(G::BAR_KVF + (nk + 1) % G::SLOTS), ((nk + 1) / G::SLOTS) & 1, g, 6)) {
                 ok = false;
                 break;
             }
         }
-        kv_base += nkv;
+        kv_base += x.nkv;
         for (int t = 0; t < x.n_qt; ++t) ++o_cnt[t];
     }
     // No MMA may still be running when TMEM is released.
@@ -301,7 +307,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     int s_cnt = 0, o_cnt = 0;
 
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit x = unit_of(u, nqb, a);
+        const Unit x = unit_of(u, nqb, nkv, a);
         if (t >= x.n_qt) continue;
         const int tile_row0 = x.m0 + t * G::BM;
         const int grow = tile_row0 + row;
@@ -312,7 +318,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         float m_ref = -INFINITY;  // reference max, log2 units
         float l = 0.f;            // running sum of 2^(s*c - m_ref)
         bool alive = true;
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = 0; j < x.nkv; ++j) {
             const bool ok = mbar_wait(bar(G::BAR_SF + t), s_cnt & 1, g, 13);
             ++s_cnt;
             if (!__all_sync(0xffffffffu, ok)) {
@@ -321,7 +327,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
             }
             tc_fence_after();
             if (warp_live) {
-                const int valid = a.sk - j * G::BN;  // keys of this tile inside [0, sk)
+                const int valid = a.sk - (x.kv0 + j) * G::BN;  // keys of this tile inside [0, sk)
                 const bool ragged = valid < G::BN;
                 uint32_t sr[G::BN];
                 const float *s = reinterpret_cast<const float *>(sr);
@@ -450,16 +456,20 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         ++o_cnt;
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
-        // Read O_t a chunk at a time, normalise, pack to 16 bits and store;
-        // then hand the accumulator back to the MMA issuer.
+        // Read O_t a chunk at a time, normalise, and store: packed to 16 bits
+        // into O, or as fp32 into this split's O_i; then hand the accumulator
+        // back to the MMA issuer.
         const float inv_l = 1.0f / l;
-        // Rows start at multiples of 2d bytes (>= 32); only the base of O may
-        // be merely 16-byte aligned.
-        const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
         const bool row_out = warp_live && grow < a.sq;
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            reinterpret_cast<uint16_t *>(a.o) +
-            ((static_cast<int64_t>(x.batch) * a.sq + (row_out ? grow : 0)) * a.h + x.head) * D);
+        const bool part = a.splits > 1;
+        // Rows start at multiples of 2d bytes (>= 32); only the base of O may
+        // be merely 16-byte aligned. The fp32 partials are allocated here.
+        const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
+        const int64_t orow =
+            ((static_cast<int64_t>(part ? x.split * a.b + x.batch : x.batch) * a.sq +
+              (row_out ? grow : 0)) * a.h + x.head) * D;
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + orow);
+        float *dst_part = a.o_part + orow;
         if (warp_live) {
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += G::OCH) {
@@ -469,7 +479,15 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 else
                     tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
                 tmem_wait_ld();
-                if (row_out) {
+                if (row_out && part) {
+#pragma unroll
+                    for (int i = 0; i < G::OCH; ++i)
+                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
+#pragma unroll
+                    for (int i = 0; i < G::OCH / 8; ++i)
+                        st_global_v8(dst_part + c0 + 8 * i,
+                                     *reinterpret_cast<const uint32_t(*)[8]>(&ov[8 * i]));
+                } else if (row_out) {
                     uint32_t pk[G::OCH / 2];
 #pragma unroll
                     for (int i = 0; i < G::OCH / 2; ++i)
@@ -493,9 +511,14 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(G::BAR_OE + t));
-        if (row_out)
-            a.lse[(static_cast<int64_t>(x.batch) * a.h + x.head) * a.sq + grow] =
-                (m_ref + __log2f(l)) * 0.69314718055994530942f;
+        if (row_out) {
+            const float lse = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+            if (part)
+                a.lse_part[((static_cast<int64_t>(x.split) * a.b + x.batch) * a.h + x.head) * a.sq +
+                           grow] = lse;
+            else
+                a.lse[(static_cast<int64_t>(x.batch) * a.h + x.head) * a.sq + grow] = lse;
+        }
     }
 }
 
@@ -513,8 +536,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const int nqb = (a.sq + G::BM * G::QT - 1) / (G::BM * G::QT);
-    const int units = nqb * a.h * a.b;
-    const int nkv = (a.sk + G::BN - 1) / G::BN;
+    const int units = nqb * a.splits * a.h * a.b;
+    const int nkv = (a.sk + G::BN - 1) / G::BN;  // key tiles in all
 
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + G::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
@@ -580,7 +603,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
         attr_set[dev] = true;
     }
     const int64_t nqb = (a.sq + G::BM * G::QT - 1) / (G::BM * G::QT);
-    const int64_t units = nqb * a.h * a.b;
+    const int64_t units = nqb * a.splits * a.h * a.b;
     const int64_t ctas = units < a.num_sms ? units : a.num_sms;
     fwd_kernel<D, BF16><<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(
         tq, tk, tv, a);

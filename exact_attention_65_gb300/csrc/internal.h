@@ -30,6 +30,14 @@ struct FwdArgs {
     uint32_t *status;
     uint32_t flags;
     int num_sms;  // persistent grid: at most one CTA per SM
+    // Split along the keys: split i covers key tiles [i * tiles_per_split,
+    // (i + 1) * tiles_per_split) and writes its normalised O_i and LSE_i to
+    // o_part [splits, b, sq, h, d] and lse_part [splits, b, h, sq] (fp32).
+    // splits == 1 writes the final o and lse.
+    int splits;
+    int tiles_per_split;
+    float *o_part;
+    float *lse_part;
 };
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
@@ -43,6 +51,11 @@ constexpr int dec_block_rows(int d) { return DEC_BLOCK_BYTES / (d * 2); }
 constexpr int dec_box_rows(int d) { return dec_block_rows(d) < 256 ? dec_block_rows(d) : 256; }
 // Query rows handled by one CTA.
 inline int dec_rows_per_cta(int sq) { return sq == 1 ? 1 : 4; }
+
+// Split count of the CUDA-core decode kernel for num_splits = 0: 1 when the
+// b * h * ceil(sq / rows per CTA) work units cover the SMs, else one CTA per
+// SM (capped by the key blocks and 128). api.cu.
+int dec_num_splits(int b, int sq, int sk, int h, int d, int num_sms);
 
 struct DecodeArgs {
     const void *q;

@@ -4,8 +4,10 @@
   include/exattn.h declares;
 * argument validation returns its status before touching any pointer;
 * the split heuristic (pure host arithmetic) follows the rule of the
-  flash-decoding issue: no split once b*h*ceil(sq/rows) work units cover
-  the SMs (b=8, h=48 gives 384 units: one split), more splits otherwise.
+  flash-decoding issue: no split once the work units cover the SMs (b=8,
+  h=48 gives 384 units: one split), more splits otherwise. A unit is
+  b*h*ceil(sq/rows) for one query row (CUDA-core kernel) and 256 query rows
+  of a (batch, head) for several (tensor-core kernel).
 """
 import ctypes
 import re
@@ -77,7 +79,7 @@ def test_fwd_validation(exattn_lib, kw, expect):
     (dict(sk=0), ea.ATTN_ERR_INVALID_ARG),
     (dict(splits=-1), ea.ATTN_ERR_INVALID_ARG),
     (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
-    (dict(b=40000, sq=8), ea.ATTN_ERR_UNSUPPORTED),      # b * ceil(sq/4) grid rows > 65535
+    (dict(b=70000), ea.ATTN_ERR_UNSUPPORTED),            # b beyond the grid limit
 ])
 def test_decode_validation(exattn_lib, kw, expect):
     assert _dec(exattn_lib, **kw) == expect
@@ -98,8 +100,14 @@ def test_heuristic_follows_the_parallel_work_rule(exattn_lib):
     # never more splits than key blocks (64 rows of d=128 per block)
     assert f(1, 1, 100, 1, 128, 148) == 2
     assert f(1, 1, 1, 1, 128, 148) == 1
-    # sq > 1: units count query blocks of 4 rows
-    assert f(2, 10, 65536, 8, 128, 148) == 148 // (2 * 8 * 3)
+    # sq > 1 runs on the tensor-core kernel: a unit is 256 query rows of one
+    # (batch, head), a split at least one 128-key tile
+    assert f(2, 10, 65536, 8, 128, 148) == 148 // (2 * 8)
+    assert f(2, 300, 65536, 8, 128, 148) == 148 // (2 * 8 * 2)
+    assert f(1, 10, 300, 16, 128, 152) == 3          # three key tiles
+    # the flash-decoding issue's workload: b8, 48 heads, 1 to 10 new rows: no split
+    for sq in range(1, 11):
+        assert f(8, sq, 8192, 48, 128, 152) == 1
     # 100 units: two splits would need 200 CTAs, more than the SMs, so one
     assert f(1, 1, 65536, 100, 128, 148) == 1
     # more work units than SMs at any sq

@@ -4,8 +4,10 @@ Shapes: the two decode problems of the flash-decoding issue (b8 h48 sk8192,
 where the heuristic must not split, and b1 h16 sk32768 with num_splits in
 {0, 2, 4, 8, 16}), plus the split/combine edge cases: more splits than key
 blocks, empty splits, a key count that is not a multiple of the block,
-several query rows, every head dim and fp16 through the explicit-dtype
-entry point. Tolerance: max |O - O_ref| <= 2e-2, max |LSE - LSE_ref| <= 1e-3.
+every head dim and fp16 through the explicit-dtype entry point. Several
+query rows (the issue's 1 to 10 new tokens, and more) run on the
+tensor-core kernel split along the keys; they get the same cases.
+Tolerance: max |O - O_ref| <= 2e-2, max |LSE - LSE_ref| <= 1e-3.
 """
 import math
 
@@ -127,3 +129,53 @@ def test_bf16_entry_point_through_raw_abi(gpu, oracle_mod):
     assert gpu.attn_get_device_status() == gpu.ATTN_OK
     o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(d))
     compare(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("sq", [2, 7, 10, 16, 130, 300])
+@pytest.mark.parametrize("splits", [0, 1, 3, 64])
+def test_many_rows_split_on_tensor_cores(gpu, oracle_mod, sq, splits):
+    """Several query rows share each K/V read: the key range is split into
+    whole 128-key tiles (3 or 64 asked; 64 exceeds the 24 tiles of sk = 3000
+    and is clamped), partials reduced by the combine kernel. sk = 3000 leaves
+    a ragged last tile; sq = 130 and 300 span two query tiles and a ragged
+    second unit."""
+    b, sk, h, d = 2, 3000, 3, 128
+    q, k, v = workloads.make_qkv(b, sq, sk, h, d, torch.bfloat16, seed=43)
+    o, lse = run_decode(gpu, q, k, v, 1 / math.sqrt(d), splits)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(d))
+    compare(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_many_rows_head_dims_and_dtypes(gpu, oracle_mod, d, dtype):
+    b, sq, sk, h = 1, 5, 1000, 4
+    q, k, v = workloads.make_qkv(b, sq, sk, h, d, dtype, seed=47)
+    for splits in (0, 1, 4):
+        o, lse = run_decode(gpu, q, k, v, 1 / math.sqrt(d), splits)
+        o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(d))
+        compare(o, lse, o_ref, lse_ref)
+
+
+def test_many_rows_split_equals_unsplit_and_forward(gpu):
+    b, sq, sk, h, d = 1, 10, 20000, 6, 128
+    q, k, v = (t.cuda() for t in workloads.make_qkv(b, sq, sk, h, d, torch.bfloat16, seed=53))
+    o0, l0 = gpu.attn_fwd(q, k, v)
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    for s in (0, 1, 2, 9, 157):
+        o1, l1 = gpu.attn_decode_splitkv(q, k, v, num_splits=s)
+        assert gpu.attn_get_device_status() == gpu.ATTN_OK
+        assert (o0.float() - o1.float()).abs().max().item() <= 1e-2
+        assert (l0 - l1).abs().max().item() <= 1e-4
+
+
+def test_issue_workload_few_new_rows(gpu, oracle_mod):
+    """The issue's decode: batch 8, 48 heads, 1 to 10 new query rows (here
+    sk = 512 to keep the oracle quick): one split, every row checked."""
+    b, sk, h, d = 8, 512, 48, 128
+    for sq in (1, 2, 10):
+        assert gpu.attn_decode_num_splits(b, sq, 8192, h, d) == 1
+        q, k, v = workloads.make_qkv(b, sq, sk, h, d, torch.bfloat16, seed=59)
+        o, lse = run_decode(gpu, q, k, v, 1 / math.sqrt(d), 0)
+        o_ref, lse_ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(d))
+        compare(o, lse, o_ref, lse_ref)

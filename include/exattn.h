@@ -67,7 +67,12 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * num_splits = 0 lets attn_decode_num_splits() choose; a positive value is
  * clamped to the number of key blocks. With one split the first kernel
  * writes O and LSE directly and no workspace is used. Any sq >= 1 is
- * accepted (non-causal). The workspace is taken stream-ordered from the
+ * accepted (non-causal). With sq == 1 the splits run on a CUDA-core kernel
+ * (key blocks of 16 KB per tensor). With sq > 1 they run on the tensor-core
+ * forward kernel, so each K/V byte is read once for all query rows of a
+ * head (the issue's case of 1 to 10 new tokens); its key blocks are tiles of
+ * 128 keys and a requested count is lowered so that no split is empty.
+ * The workspace is taken stream-ordered from the
  * device's default memory pool and returned after the reduce; it is kept
  * cached in the pool until attn_release_workspace().
  */
@@ -119,9 +124,11 @@ attn_status_t attn_decode_splitkv_noalloc(const void *q, const void *k, const vo
 
 /*
  * The split heuristic for num_splits = 0 on the current device (same issue:
- * split only when the b * h * ceil(sq / rows per CTA) work units leave SMs
- * idle). Returns the split count (>= 1), or 0 on invalid sizes or when no
- * device can be queried.
+ * split only when the work units leave SMs idle; then one CTA per SM, at
+ * most one split per key block and 128 splits). A work unit is one query
+ * row of a (batch, head) when sq == 1, and 256 query rows of a (batch,
+ * head) when sq > 1. Returns the split count (>= 1), or 0 on invalid sizes
+ * or when no device can be queried.
  */
 int attn_decode_num_splits(int b, int sq, int sk, int h, int d);
 

@@ -122,23 +122,31 @@ struct Unit {
     int m0, head, batch, n_qt, split, kv0, nkv;
 };
 
-// Units are numbered query block first, then split, head and batch.
+// Units are numbered query block first, then split, head and batch. The
+// kernel is compiled with and without key splits (SPLIT): the plain forward
+// keeps the shorter code.
+template <bool SPLIT>
 __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdArgs &a) {
     Unit x;
     const int qb = u % nqb;
     int r = u / nqb;
-    x.split = r % a.splits;
-    r /= a.splits;
+    x.split = 0;
+    x.kv0 = 0;
+    x.nkv = nkv_all;
+    if constexpr (SPLIT) {
+        x.split = r % a.splits;
+        r /= a.splits;
+        x.kv0 = x.split * a.tiles_per_split;
+        x.nkv = min(a.tiles_per_split, nkv_all - x.kv0);
+    }
     x.head = r % a.h;
     x.batch = r / a.h;
     x.m0 = qb * (FWD_BM * FWD_QTILES);
     x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
-    x.kv0 = x.split * a.tiles_per_split;
-    x.nkv = min(a.tiles_per_split, nkv_all - x.kv0);
     return x;
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                              const CUtensorMap *tv, uint32_t sbase, int nqb,
                                              int units, int nkv, const FwdArgs &a,
@@ -150,7 +158,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     int q_issued = 0, n_issued = 0;  // n counts ring items (K and V tiles)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const Unit x = unit_of(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
         // A Q buffer is free once every S MMA of the unit two back has completed.
         const int qb = q_issued % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QE + qb), ((q_issued / G::QBUF) & 1) ^ 1, g, 1)) break;
@@ -189,7 +197,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
         mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, int units,
                                         int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
@@ -211,7 +219,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     int o_cnt[G::QT] = {};  // units finished per query tile
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
-        const Unit x = unit_of(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
         const int qbuf = it_u % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QF + qbuf), (it_u / G::QBUF) & 1, g, 4)) break;
         // The issue order keeps the tensor core's short instruction queue fed:
@@ -292,7 +300,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4, int nqb,
                                             int units, int nkv, const FwdArgs &a,
                                             const WaitGuard &g) {
@@ -307,7 +315,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     int s_cnt = 0, o_cnt = 0;
 
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit x = unit_of(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
         if (t >= x.n_qt) continue;
         const int tile_row0 = x.m0 + t * G::BM;
         const int grow = tile_row0 + row;
@@ -461,7 +469,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         // back to the MMA issuer.
         const float inv_l = 1.0f / l;
         const bool row_out = warp_live && grow < a.sq;
-        const bool part = a.splits > 1;
+        constexpr bool part = SPLIT;
         // Rows start at multiples of 2d bytes (>= 32); only the base of O may
         // be merely 16-byte aligned. The fp32 partials are allocated here.
         const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
@@ -479,7 +487,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 else
                     tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
                 tmem_wait_ld();
-                if (row_out && part) {
+                if (part && row_out) {
 #pragma unroll
                     for (int i = 0; i < G::OCH; ++i)
                         ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
@@ -513,7 +521,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         if (lane == 0) mbar_arrive(bar(G::BAR_OE + t));
         if (row_out) {
             const float lse = (m_ref + __log2f(l)) * 0.69314718055994530942f;
-            if (part)
+            if constexpr (part)
                 a.lse_part[((static_cast<int64_t>(x.split) * a.b + x.batch) * a.h + x.head) * a.sq +
                            grow] = lse;
             else
@@ -522,7 +530,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -573,13 +581,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         reg_dealloc<kRegsControl>();
         if (warp == 0) {
             if (lane == 0 && !(a.flags & kFlagSkipLoads))
-                fwd_producer<D>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+                fwd_producer<D, SPLIT>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
         } else if (warp == 1) {
-            if (lane == 0) fwd_mma<D, BF16>(sbase, tmem, nqb, units, nkv, a, g);
+            if (lane == 0) fwd_mma<D, BF16, SPLIT>(sbase, tmem, nqb, units, nkv, a, g);
         }
     } else {
         reg_alloc<kRegsSoftmax>();
-        fwd_softmax<D, BF16>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv, a, g);
+        fwd_softmax<D, BF16, SPLIT>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv, a, g);
     }
 
     tc_fence_before();
@@ -588,7 +596,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
     using G = FwdGeom<D>;
@@ -597,17 +605,24 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 G::SMEM_BYTES);
+        e = cudaFuncSetAttribute(fwd_kernel<D, BF16, SPLIT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const int64_t nqb = (a.sq + G::BM * G::QT - 1) / (G::BM * G::QT);
     const int64_t units = nqb * a.splits * a.h * a.b;
     const int64_t ctas = units < a.num_sms ? units : a.num_sms;
-    fwd_kernel<D, BF16><<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(
-        tq, tk, tv, a);
+    fwd_kernel<D, BF16, SPLIT>
+        <<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const FwdArgs &a, cudaStream_t stream) {
+    return a.splits > 1 ? launch_fwd_t<D, BF16, true>(tq, tk, tv, a, stream)
+                        : launch_fwd_t<D, BF16, false>(tq, tk, tv, a, stream);
 }
 
 }  // namespace
@@ -616,8 +631,8 @@ cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMa
                        const CUtensorMap &tv, const FwdArgs &a, cudaStream_t stream) {
 #define EXATTN_FWD_CASE(DD)                                               \
     case DD:                                                              \
-        return bf16 ? launch_fwd_t<DD, true>(tq, tk, tv, a, stream)       \
-                    : launch_fwd_t<DD, false>(tq, tk, tv, a, stream);
+        return bf16 ? launch_fwd_d<DD, true>(tq, tk, tv, a, stream)       \
+                    : launch_fwd_d<DD, false>(tq, tk, tv, a, stream);
     switch (d) {
         EXATTN_FWD_CASE(16)
         EXATTN_FWD_CASE(32)

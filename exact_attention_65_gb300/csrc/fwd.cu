@@ -370,10 +370,16 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                             tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
                     }
                     tmem_wait_ld();
+                    // whole 32-key chunks past sk are skipped (a warp-uniform branch)
 #pragma unroll
-                    for (int i = 0; i < G::BN; ++i) {
-                        if (i < valid)
-                            mx[i & 3] = c_pos ? fmaxf(mx[i & 3], s[i]) : fminf(mx[i & 3], s[i]);
+                    for (int c0 = 0; c0 < G::BN; c0 += 32) {
+                        if (c0 < valid) {
+#pragma unroll
+                            for (int i = c0; i < c0 + 32; ++i) {
+                                if (i < valid)
+                                    mx[i & 3] = c_pos ? fmaxf(mx[i & 3], s[i]) : fminf(mx[i & 3], s[i]);
+                            }
+                        }
                     }
                 }
                 const float mraw = c_pos ? fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3])
@@ -413,18 +419,28 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                             pk[i] = pack2<BF16>(p0, p1);
                         }
                     } else {
-                        // last key tile: keys past sk are masked to exactly 0
+                        // last key tile: keys past sk are masked to exactly 0; whole
+                        // 32-key chunks past sk are zero without exponentiating (a
+                        // warp-uniform branch)
 #pragma unroll
-                        for (int i = 0; i < G::BN / 4; ++i) {
-                            const int k0 = half * (G::BN / 2) + 2 * i;
-                            float x0, x1;
-                            f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
-                            x0 = (k0 < valid) ? x0 : -INFINITY;
-                            x1 = (k0 + 1 < valid) ? x1 : -INFINITY;
-                            const float p0 = fast_exp2(x0);
-                            const float p1 = fast_exp2(x1);
-                            acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
-                            pk[i] = pack2<BF16>(p0, p1);
+                        for (int ch = 0; ch < 2; ++ch) {
+                            if (half * (G::BN / 2) + ch * 32 < valid) {
+#pragma unroll
+                                for (int i = ch * 16; i < ch * 16 + 16; ++i) {
+                                    const int k0 = half * (G::BN / 2) + 2 * i;
+                                    float x0, x1;
+                                    f2_split(f2_fma(f2_make(s[k0], s[k0 + 1]), c2, nm2), x0, x1);
+                                    x0 = (k0 < valid) ? x0 : -INFINITY;
+                                    x1 = (k0 + 1 < valid) ? x1 : -INFINITY;
+                                    const float p0 = fast_exp2(x0);
+                                    const float p1 = fast_exp2(x1);
+                                    acc2[i & 1] = f2_add(acc2[i & 1], f2_make(p0, p1));
+                                    pk[i] = pack2<BF16>(p0, p1);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = ch * 16; i < ch * 16 + 16; ++i) pk[i] = 0u;
+                            }
                         }
                     }
                     tmem_st32(tS + half * (G::BN / 4), pk);

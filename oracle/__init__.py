@@ -51,7 +51,7 @@ def _load():
             vp, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             lib.oracle_attn.restype = i32
             lib.oracle_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, dbl,
-                                        i32, i32, vp, i32, vp, vp]
+                                        i32, i32, i32, vp, i32, vp, vp]
             lib.oracle_combine.restype = i32
             lib.oracle_combine.argtypes = [vp, vp, i32, ctypes.c_int64, i32, vp, vp]
             lib.oracle_f16_to_f64.restype = dbl
@@ -96,13 +96,16 @@ def _as_raw(x):
     raise TypeError(f"unsupported dtype {a.dtype}")
 
 
-def attention(q, k, v, scale: float, rows=None, key_range=None):
+def attention(q, k, v, scale: float, rows=None, key_range=None, causal=False):
     """Exact attention in fp64.
 
     q: [b, sq, h, d]; k, v: [b, sk, h, d] (torch CPU tensors or numpy arrays,
     fp64/fp32/fp16/bf16; all three the same dtype).
     rows: optional list of query rows to evaluate (default: all sq).
     key_range: optional (j0, j1); only keys j0 <= j < j1 take part.
+    causal: bottom-right-aligned causal mask (not on the pages; the common
+    reading): query row i sees key j only if j <= i + sk - sq. A row left
+    with no key gives O = 0 and LSE = -inf.
     Returns (o [b, nrows, h, d], lse [b, h, nrows]) as float64 numpy arrays.
     """
     qa, dt = _as_raw(q)
@@ -124,7 +127,7 @@ def attention(q, k, v, scale: float, rows=None, key_range=None):
     o = np.empty((b, nrows, h, d), dtype=np.float64)
     lse = np.empty((b, h, nrows), dtype=np.float64)
     rc = _load().oracle_attn(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dt,
-                             b, sq, sk, h, d, float(scale), int(j0), int(j1),
+                             b, sq, sk, h, d, float(scale), int(j0), int(j1), int(bool(causal)),
                              rows_ptr, nrows, o.ctypes.data, lse.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_attn rejected its arguments")
@@ -151,12 +154,12 @@ def combine(o_parts, lse_parts):
     return o, lse
 
 
-def split_attention(q, k, v, scale: float, bounds, rows=None):
+def split_attention(q, k, v, scale: float, bounds, rows=None, causal=False):
     """Per-split (O_i, LSE_i) over the key ranges ``bounds`` = [(j0, j1), ...],
     combined by ``combine``. Returns (o [b, nrows, h, d], lse [b, h, nrows])."""
     parts_o, parts_l = [], []
     for (j0, j1) in bounds:
-        o_i, l_i = attention(q, k, v, scale, rows=rows, key_range=(j0, j1))
+        o_i, l_i = attention(q, k, v, scale, rows=rows, key_range=(j0, j1), causal=causal)
         b, nr, h, d = o_i.shape
         # put both in (b, h, row) order for the reduce
         parts_o.append(o_i.transpose(0, 2, 1, 3).reshape(b * h * nr, d))

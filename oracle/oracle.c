@@ -21,6 +21,12 @@
  *    flash-decoding issue ("where is flash decoding second stage (reduce)
  *    code?"). An empty key range gives LSE = -inf and O = 0, the identity
  *    of the combine below.
+ *    Causal masking is not on the pages. With `causal` set, the reading
+ *    used is the bottom-right-aligned mask: query row i (of sq) sees key j
+ *    (of sk) only if j <= i + sk - sq, so the last query row sees every key
+ *    and, with sq == sk, row i sees keys 0..i. That only shortens row i's
+ *    key range; a row left with no key is an empty range (O = 0,
+ *    LSE = -inf).
  *
  *  oracle_combine -- the second (reduce) stage of split-KV decoding, from
  *    the same flash-decoding issue: with the max of the split LSEs taken out
@@ -82,13 +88,14 @@ static double load(const void *p, int dtype, int64_t i) {
 /*
  * q: [b, sq, h, d]; k, v: [b, sk, h, d] (contiguous, d innermost).
  * rows: the query rows to evaluate (nrows of them), or NULL for 0..sq-1.
- * Keys j0 <= j < j1 take part.
+ * Keys j0 <= j < j1 take part; with causal != 0, row i also only keys
+ * j <= i + sk - sq.
  * o: [b, nrows, h, d] fp64; lse: [b, h, nrows] fp64.
  * Returns 0, or -1 on a bad argument or allocation failure.
  */
 int oracle_attn(const void *q, const void *k, const void *v, int dtype,
                 int b, int sq, int sk, int h, int d, double scale,
-                int j0, int j1, const int32_t *rows, int nrows,
+                int j0, int j1, int causal, const int32_t *rows, int nrows,
                 double *o, double *lse) {
     if (b < 0 || sq < 0 || sk < 0 || h < 0 || d <= 0 || j0 < 0 || j1 > sk || j0 > j1)
         return -1;
@@ -99,8 +106,8 @@ int oracle_attn(const void *q, const void *k, const void *v, int dtype,
 
 #pragma omp parallel reduction(| : failed)
     {
-        int n = j1 - j0;
-        double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
+        const int n_all = j1 - j0;
+        double *s = (double *)malloc(sizeof(double) * (n_all > 0 ? n_all : 1));
         double *acc = (double *)malloc(sizeof(double) * d);
         {
 #pragma omp for schedule(dynamic, 16)
@@ -118,6 +125,12 @@ int oracle_attn(const void *q, const void *k, const void *v, int dtype,
                 if (i < 0 || i >= sq) {
                     failed = 1;
                     continue;
+                }
+                int n = n_all;
+                if (causal) {
+                    /* keys j0 .. min(j1, i + sk - sq + 1) - 1 */
+                    const int64_t end = (int64_t)i + sk - sq + 1;
+                    n = end <= j0 ? 0 : (end < j1 ? (int)(end - j0) : n_all);
                 }
                 if (n == 0) {
                     for (int t = 0; t < d; ++t) orow[t] = 0.0;

@@ -257,3 +257,99 @@ def test_narrow_inputs_match_widened(oracle_mod, dtype):
     o64, lse64 = oracle_mod.attention(q.double(), k.double(), v.double(), 0.25)
     np.testing.assert_array_equal(o, o64)
     np.testing.assert_array_equal(lse, lse64)
+
+
+# ---------------------------------------------------------------- causal mask
+# Not on the pages; the reading is the bottom-right-aligned mask: query row i
+# (of sq) sees key j (of sk) only if j <= i + sk - sq. Rows left with no key
+# give O = 0 and LSE = -inf (the empty-range convention of the combine).
+def _bottom_right_mask(sq, sk):
+    i = np.arange(sq)[:, None]
+    j = np.arange(sk)[None, :]
+    return j <= i + (sk - sq)
+
+
+def _torch_masked(q, k, v, scale, mask):
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (q, k, v))  # (b, h, s, d)
+    m = torch.from_numpy(mask)
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=m, scale=scale)
+    sc = (scale * tq @ tk.transpose(-1, -2)).masked_fill(~m, float("-inf"))
+    return o.transpose(1, 2).numpy(), torch.logsumexp(sc, dim=-1).numpy()
+
+
+def test_causal_square_is_torch_is_causal(oracle_mod):
+    b, s, h, d, scale = 2, 11, 3, 8, 0.41
+    q, k, v = _rand((b, s, h, d), 21), _rand((b, s, h, d), 22), _rand((b, s, h, d), 23)
+    o, lse = oracle_mod.attention(q, k, v, scale, causal=True)
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=scale)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+    _, ref_lse = _torch_masked(q, k, v, scale, _bottom_right_mask(s, s))
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("sq,sk", [(5, 13), (1, 7), (13, 13), (9, 4), (4, 1)])
+def test_causal_rectangular_is_torch_bottom_right_mask(oracle_mod, sq, sk):
+    b, h, d, scale = 2, 2, 6, 0.7
+    q, k, v = _rand((b, sq, h, d), 24), _rand((b, sk, h, d), 25), _rand((b, sk, h, d), 26)
+    o, lse = oracle_mod.attention(q, k, v, scale, causal=True)
+    mask = _bottom_right_mask(sq, sk)
+    seen = mask.any(axis=1)  # rows with at least one key
+    ro, rl = _torch_masked(q, k, v, scale, mask)
+    np.testing.assert_allclose(o[:, seen], ro[:, seen], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[:, :, seen], rl[:, :, seen], rtol=0, atol=1e-12)
+    # rows with no key: the empty-range convention
+    assert np.all(o[:, ~seen] == 0.0)
+    assert np.all(np.isneginf(lse[:, :, ~seen]))
+    assert (~seen).sum() == max(0, sq - sk)
+
+
+def _brute_causal(q, k, v, scale):
+    b, sq, h, d = q.shape
+    sk = k.shape[1]
+    o = np.zeros((b, sq, h, d))
+    lse = np.full((b, h, sq), -np.inf)
+    for bb in range(b):
+        for hh in range(h):
+            for i in range(sq):
+                keys = [j for j in range(sk) if j - i <= sk - sq]
+                if not keys:
+                    continue
+                e = [math.exp(scale * math.fsum(q[bb, i, hh, t] * k[bb, j, hh, t] for t in range(d)))
+                     for j in keys]
+                z = math.fsum(e)
+                for t in range(d):
+                    o[bb, i, hh, t] = math.fsum(e[n] / z * v[bb, j, hh, t] for n, j in enumerate(keys))
+                lse[bb, hh, i] = math.log(z)
+    return o, lse
+
+
+@pytest.mark.parametrize("shape,scale", [((1, 3, 6, 2, 4), 0.5), ((2, 6, 3, 1, 3), -0.8),
+                                         ((1, 4, 4, 2, 2), 1.1)])
+def test_causal_brute_force(oracle_mod, shape, scale):
+    b, sq, sk, h, d = shape
+    q, k, v = _rand((b, sq, h, d), 27), _rand((b, sk, h, d), 28), _rand((b, sk, h, d), 29)
+    o, lse = oracle_mod.attention(q, k, v, scale, causal=True)
+    ob, lb = _brute_causal(q, k, v, scale)
+    np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def test_causal_single_query_row_sees_every_key(oracle_mod):
+    b, sk, h, d = 2, 17, 3, 5
+    q, k, v = _rand((b, 1, h, d), 30), _rand((b, sk, h, d), 31), _rand((b, sk, h, d), 32)
+    o0, l0 = oracle_mod.attention(q, k, v, 0.3)
+    o1, l1 = oracle_mod.attention(q, k, v, 0.3, causal=True)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+@pytest.mark.parametrize("bounds", [[(0, 5), (5, 12), (12, 20)], [(0, 20), (20, 20)],
+                                    [(0, 1), (1, 2), (2, 20)]])
+def test_causal_split_combine_equals_unsplit(oracle_mod, bounds):
+    b, sq, sk, h, d = 1, 8, 20, 2, 4
+    q, k, v = _rand((b, sq, h, d), 33), _rand((b, sk, h, d), 34), _rand((b, sk, h, d), 35)
+    o, lse = oracle_mod.attention(q, k, v, 0.6, causal=True)
+    o2, l2 = oracle_mod.split_attention(q, k, v, 0.6, bounds, causal=True)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, lse, rtol=0, atol=1e-12)

@@ -62,6 +62,11 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_splitkv_ex.restype = i32
         lib.attn_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp]
+        lib.attn_fwd_causal.restype = i32
+        lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_decode_splitkv_causal.restype = i32
+        lib.attn_decode_splitkv_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                   f32, i32, i32, vp]
         lib.attn_decode_num_splits.restype = i32
         lib.attn_decode_num_splits.argtypes = [i32] * 5
         lib.attn_decode_num_splits_for_sms.restype = i32
@@ -131,26 +136,29 @@ def _stream(device, stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=None):
+def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=None,
+             causal: bool = False):
     """Exact attention O = softmax(scale * Q K^T) V and LSE [b, h, sq] (fp32).
 
     q: [b, sq, h, d], k/v: [b, sk, h, d], fp16 or bf16, contiguous CUDA
     tensors; default scale 1/sqrt(d). Runs on ``stream`` (default: the
-    current stream of q's device)."""
+    current stream of q's device). ``causal``: bottom-right-aligned mask
+    (query row i sees key j only if j <= i + sk - sq)."""
     b, sq, sk, h, d, dt = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, b, h, sq)
     lib = load_library()
+    fn = lib.attn_fwd_causal if causal else lib.attn_fwd
     with torch.cuda.device(q.device):
-        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                          b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd")
+        raise AttnError(rc, "attn_fwd_causal" if causal else "attn_fwd")
     return out, lse
 
 
 def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0, out=None,
-                        lse=None, stream=None):
+                        lse=None, stream=None, causal: bool = False):
     """Split-KV decode: same result as attn_fwd, computed by splitting the
     keys into ``num_splits`` ranges (0 = heuristic) and reducing the
     per-split (O_i, LSE_i) with the log-sum-exp combine."""
@@ -158,10 +166,10 @@ def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, b, h, sq)
     lib = load_library()
+    fn = lib.attn_decode_splitkv_causal if causal else lib.attn_decode_splitkv_ex
     with torch.cuda.device(q.device):
-        rc = lib.attn_decode_splitkv_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                        lse.data_ptr(), b, sq, sk, h, d, scale, int(num_splits), dt,
-                                        _stream(q.device, stream))
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                b, sq, sk, h, d, scale, int(num_splits), dt, _stream(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_splitkv")
     return out, lse

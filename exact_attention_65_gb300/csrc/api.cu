@@ -148,7 +148,7 @@ attn_status_t alloc_partials(int64_t splits, int b, int sq, int h, int d, cudaSt
 // so that no split is empty.
 attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b,
                       int sq, int sk, int h, int d, float scale, bool bf16, int64_t splits,
-                      const DeviceState *ds, cudaStream_t stream) {
+                      bool causal, const DeviceState *ds, cudaStream_t stream) {
     const int64_t nkv = cdiv(sk, FWD_BN);
     if (splits > nkv) splits = nkv;
     if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
@@ -179,6 +179,7 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     a.tiles_per_split = static_cast<int>(tps);
     a.o_part = nullptr;
     a.lse_part = nullptr;
+    a.causal = causal ? 1 : 0;
     if (splits == 1)
         return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     void *ws = nullptr;
@@ -240,7 +241,19 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     if (st != ATTN_OK) return st;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
-    return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, 1, ds, stream);
+    return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, 1, false, ds,
+                   stream);
+}
+
+attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                              cudaStream_t stream) {
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, 1, true, ds,
+                   stream);
 }
 
 int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms) {
@@ -280,7 +293,7 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
         const int64_t s = num_splits == 0
                               ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms)
                               : num_splits;
-        return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, bf16, s, ds, stream);
+        return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, bf16, s, false, ds, stream);
     }
     const int64_t nblocks = cdiv(sk, dec_block_rows(d));
     int64_t splits = num_splits == 0
@@ -322,6 +335,26 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const void *v, void *o,
+                                         float *lse, int b, int sq, int sk, int h, int d,
+                                         float scale, int num_splits, attn_dtype_t dtype,
+                                         cudaStream_t stream) {
+    // One query row sees every key under the bottom-right-aligned mask.
+    if (sq == 1)
+        return attn_decode_splitkv_ex(q, k, v, o, lse, b, sq, sk, h, d, scale, num_splits, dtype,
+                                      stream);
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    const int64_t s = num_splits == 0
+                          ? attn_decode_num_splits_for_sms(b, sq, sk, h, d, ds->num_sms)
+                          : num_splits;
+    return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, s, true, ds,
+                   stream);
 }
 
 attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,

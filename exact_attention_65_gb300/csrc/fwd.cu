@@ -143,6 +143,16 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     x.batch = r / a.h;
     x.m0 = qb * (FWD_BM * FWD_QTILES);
     x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
+    if constexpr (SPLIT) {
+        if (a.causal) {
+            // the unit's last row sees keys up to last + sk - sq: later key
+            // tiles are not needed (none at all if that is below 0)
+            const int last = min(x.m0 + FWD_BM * FWD_QTILES, a.sq) - 1;
+            const int kmax = last + a.sk - a.sq;
+            const int tiles = kmax < 0 ? 0 : kmax / FWD_BN + 1;
+            x.nkv = max(0, min(x.nkv, tiles - x.kv0));
+        }
+    }
     return x;
 }
 
@@ -289,6 +299,9 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                 break;
             }
         }
+        // a unit with no key tile (causal) still frees its Q buffer
+        if constexpr (SPLIT)
+            if (x.nkv == 0) mma_commit(bar(G::BAR_QE + qbuf));
         kv_base += x.nkv;
         for (int t = 0; t < x.n_qt; ++t) ++o_cnt[t];
     }
@@ -335,8 +348,19 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
             }
             tc_fence_after();
             if (warp_live) {
-                const int valid = a.sk - (x.kv0 + j) * G::BN;  // keys of this tile inside [0, sk)
-                const bool ragged = valid < G::BN;
+                // keys of this tile the row may use: inside [0, sk) and, with the
+                // causal mask, at most grow + sk - sq. Loads and chunk skips
+                // follow the warp's largest count (tcgen05.ld is warp-wide).
+                int valid = a.sk - (x.kv0 + j) * G::BN;
+                int vmax = valid;
+                bool ragged = valid < G::BN;
+                if constexpr (SPLIT) {
+                    if (a.causal) {
+                        valid = min(valid, grow + a.sk - a.sq + 1 - (x.kv0 + j) * G::BN);
+                        vmax = __reduce_max_sync(0xffffffffu, valid);
+                        ragged = __any_sync(0xffffffffu, valid < G::BN);
+                    }
+                }
                 uint32_t sr[G::BN];
                 const float *s = reinterpret_cast<const float *>(sr);
                 // row max of the scaled scores (min of the raw ones if scale < 0)
@@ -366,14 +390,14 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 } else {
 #pragma unroll
                     for (int c0 = 0; c0 < G::BN; c0 += 32) {
-                        if (c0 < valid)
+                        if (c0 < vmax)
                             tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
                     }
                     tmem_wait_ld();
                     // whole 32-key chunks past sk are skipped (a warp-uniform branch)
 #pragma unroll
                     for (int c0 = 0; c0 < G::BN; c0 += 32) {
-                        if (c0 < valid) {
+                        if (c0 < vmax) {
 #pragma unroll
                             for (int i = c0; i < c0 + 32; ++i) {
                                 if (i < valid)
@@ -388,7 +412,10 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
 
                 const bool need = m_tile > m_ref + 8.0f;
                 const float m_new = need ? m_tile : m_ref;
-                const float alpha = fast_exp2(m_ref - m_new);  // 1 if kept, 0 on the first tile
+                // 1 if kept, 0 on the first tile; a row that has seen no key yet
+                // (causal) keeps m = -inf and alpha 1
+                const float alpha =
+                    (SPLIT && m_new == -INFINITY) ? 1.0f : fast_exp2(m_ref - m_new);
                 m_ref = m_new;
 
                 // O must be rescaled (rare once the running max settles) before
@@ -424,7 +451,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                         // warp-uniform branch)
 #pragma unroll
                         for (int ch = 0; ch < 2; ++ch) {
-                            if (half * (G::BN / 2) + ch * 32 < valid) {
+                            if (half * (G::BN / 2) + ch * 32 < vmax) {
 #pragma unroll
                                 for (int i = ch * 16; i < ch * 16 + 16; ++i) {
                                     const int k0 = half * (G::BN / 2) + 2 * i;
@@ -483,9 +510,13 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         // Read O_t a chunk at a time, normalise, and store: packed to 16 bits
         // into O, or as fp32 into this split's O_i; then hand the accumulator
         // back to the MMA issuer.
-        const float inv_l = 1.0f / l;
+        // A row that saw no key (causal) has l = 0: O = 0, LSE = -inf.
+        const bool empty_row = SPLIT && !(l > 0.0f);
+        const float inv_l = empty_row ? 0.0f : 1.0f / l;
         const bool row_out = warp_live && grow < a.sq;
-        constexpr bool part = SPLIT;
+        // fp32 partials only with more than one split (the SPLIT instantiation
+        // also runs causal calls with one split, which write O and LSE)
+        const bool part = SPLIT && a.splits > 1;
         // Rows start at multiples of 2d bytes (>= 32); only the base of O may
         // be merely 16-byte aligned. The fp32 partials are allocated here.
         const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
@@ -506,7 +537,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 if (part && row_out) {
 #pragma unroll
                     for (int i = 0; i < G::OCH; ++i)
-                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
+                        ov[i] = empty_row ? 0u : __float_as_uint(__uint_as_float(ov[i]) * inv_l);
 #pragma unroll
                     for (int i = 0; i < G::OCH / 8; ++i)
                         st_global_v8(dst_part + c0 + 8 * i,
@@ -515,8 +546,9 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                     uint32_t pk[G::OCH / 2];
 #pragma unroll
                     for (int i = 0; i < G::OCH / 2; ++i)
-                        pk[i] = pack2<BF16>(__uint_as_float(ov[2 * i]) * inv_l,
-                                            __uint_as_float(ov[2 * i + 1]) * inv_l);
+                        pk[i] = empty_row ? 0u
+                                          : pack2<BF16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
                     if (o_al32) {
                         // whole 32-byte sectors: 16 columns per store
 #pragma unroll
@@ -536,8 +568,9 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(G::BAR_OE + t));
         if (row_out) {
-            const float lse = (m_ref + __log2f(l)) * 0.69314718055994530942f;
-            if constexpr (part)
+            const float lse =
+                empty_row ? -INFINITY : (m_ref + __log2f(l)) * 0.69314718055994530942f;
+            if (part)
                 a.lse_part[((static_cast<int64_t>(x.split) * a.b + x.batch) * a.h + x.head) * a.sq +
                            grow] = lse;
             else
@@ -637,8 +670,8 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 template <int D, bool BF16>
 cudaError_t launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
-    return a.splits > 1 ? launch_fwd_t<D, BF16, true>(tq, tk, tv, a, stream)
-                        : launch_fwd_t<D, BF16, false>(tq, tk, tv, a, stream);
+    return (a.splits > 1 || a.causal) ? launch_fwd_t<D, BF16, true>(tq, tk, tv, a, stream)
+                                      : launch_fwd_t<D, BF16, false>(tq, tk, tv, a, stream);
 }
 
 }  // namespace

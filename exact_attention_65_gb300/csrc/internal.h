@@ -38,6 +38,9 @@ struct FwdArgs {
     int tiles_per_split;
     float *o_part;
     float *lse_part;
+    // Causal mask, bottom-right aligned: query row i sees key j only if
+    // j <= i + sk - sq; rows that see no key get O = 0 and LSE = -inf.
+    int causal;
 };
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -59,6 +59,19 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_fwd with a causal mask. Causal masking is not on the pages; the mask
+ * is the bottom-right-aligned one: query row i (of sq) sees key j (of sk)
+ * only if j <= i + sk - sq, so with sq == sk row i sees keys 0..i, and with
+ * sq < sk the last query row sees every key (new tokens appended to a
+ * cache). Rows that see no key (i < sq - sk) get O = 0 and LSE = -inf.
+ * Key tiles wholly past a query tile's last visible key are skipped.
+ * Arguments, layouts and errors are those of attn_fwd.
+ */
+attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int b, int sq, int sk, int h, int d, float scale,
+                              attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * Split-KV decode, bf16 q/k/v/o ("where is flash decoding second stage
  * (reduce) code?" issue). seqlen_k is cut into num_splits ranges of whole
  * key blocks; split i writes its own O_i and LSE_i (fp32, library
@@ -84,6 +97,17 @@ attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, v
 attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                                      int b, int sq, int sk, int h, int d, float scale,
                                      int num_splits, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * attn_decode_splitkv_ex with the causal mask of attn_fwd_causal (bottom-right
+ * aligned: the sq new query rows are the last sq positions of the sk keys).
+ * With sq == 1 it is attn_decode_splitkv_ex. Splits wholly past a query
+ * row's last visible key contribute nothing to it (LSE_i = -inf).
+ */
+attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const void *v, void *o,
+                                         float *lse, int b, int sq, int sk, int h, int d,
+                                         float scale, int num_splits, attn_dtype_t dtype,
+                                         cudaStream_t stream);
 
 /*
  * Split-KV decode that allocates no device memory. The pages have no

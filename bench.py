@@ -383,6 +383,33 @@ def measure_extras(ea, dev, flush, stream, peaks):
                      "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
                      "GB/s": round(w.io_bytes / (ms * 1e-3) / 1e9, 1)}
         del q, k, v
+    # causal forward (bottom-right aligned; sq == sk here): FLOP counts only
+    # the unmasked scores, 4*b*h*d * sum over rows of the keys a row sees
+    for name in ("mid_fwd", "long_fwd"):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        fn = lambda: ea.attn_fwd(q, k, v, scale=w.scale, causal=True)  # noqa: E731
+        (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+        flops = 4 * w.b * w.h * w.d * (w.sq * (w.sq + 1) // 2)
+        tf = flops / (ms * 1e-3) / 1e12
+        out[f"{name}/causal"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                                 "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v
+    # several new query rows share each K/V read (tensor-core decode path)
+    for name, sq in (("decode_b8_h48_sk8192", 10), ("decode_b1_h16_sk32768", 10)):
+        w = workloads.WORKLOADS[name]
+        gen_q = torch.randn((w.b, sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        _, k, v = rand(w)
+        for causal in (False, True):
+            fn = lambda: ea.attn_decode_splitkv(gen_q, k, v, scale=w.scale,  # noqa: E731
+                                                causal=causal)
+            (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+            kv = 2 * k.numel() * k.element_size()
+            gbs = kv / (ms * 1e-3) / 1e9
+            tag = "/causal" if causal else ""
+            out[f"{name}/sq={sq}{tag}"] = {"ms": round(ms, 5), "GB/s (K+V)": round(gbs, 1),
+                                           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del k, v, gen_q
     for name, split_list in (("decode_b8_h48_sk8192", [0]),
                              ("decode_b1_h16_sk32768", [0, 1, 2, 4, 8, 16])):
         w = workloads.WORKLOADS[name]

@@ -128,8 +128,12 @@ struct Unit {
 template <bool SPLIT>
 __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdArgs &a) {
     Unit x;
-    const int qb = u % nqb;
+    int qb = u % nqb;
     int r = u / nqb;
+    // Causal units grow with the query block. Running every other group's
+    // query blocks in reverse order mixes heavy and light units in each CTA's
+    // strided share.
+    if (SPLIT && a.causal && (r & 1)) qb = nqb - 1 - qb;
     x.split = 0;
     x.kv0 = 0;
     x.nkv = nkv_all;

@@ -175,3 +175,43 @@ def decode_f16(bits: int) -> float:
 
 def decode_bf16(bits: int) -> float:
     return _load().oracle_bf16_to_f64(bits)
+
+
+def paged_attention(q, k_pages, v_pages, block_table, seqlens, scale: float):
+    """Exact attention of each sequence's query rows over its own keys, read
+    through a page table (a paged KV cache; the pages only mention one, so
+    the layout is the common one): key r of sequence i is row r % page_size
+    of pool page block_table[i, r // page_size], and sequence i has
+    seqlens[i] keys. The keys are gathered into one contiguous cache per
+    sequence and passed to ``attention``; a sequence with no key gives O = 0
+    and LSE = -inf.
+
+    q: [b, sq, h, d]; k_pages, v_pages: [num_pages, page_size, h, d];
+    block_table: [b, max_pages] ints; seqlens: [b] ints (CPU tensors or
+    numpy arrays). Returns (o [b, sq, h, d], lse [b, h, sq]) fp64."""
+    table = np.asarray(block_table)
+    lens = np.asarray(seqlens)
+    page_size = k_pages.shape[1]
+    outs_o, outs_l = [], []
+    for i in range(q.shape[0]):
+        n = int(lens[i])
+        npg = (n + page_size - 1) // page_size
+        if n == 0:
+            keys = [int(table[i, 0])]  # any one page; the key range below is empty
+        else:
+            keys = [int(table[i, p]) for p in range(npg)]
+        kc = _stack_pages(k_pages, keys)
+        vc = _stack_pages(v_pages, keys)
+        o_i, l_i = attention(q[i:i + 1], kc, vc, scale, key_range=(0, n))
+        outs_o.append(o_i)
+        outs_l.append(l_i)
+    return np.concatenate(outs_o, axis=0), np.concatenate(outs_l, axis=0)
+
+
+def _stack_pages(pool, pages):
+    """[1, len(pages) * page_size, h, d]: the listed pool pages in order."""
+    if isinstance(pool, np.ndarray):
+        return np.concatenate([pool[p] for p in pages], axis=0)[None]
+    import torch
+
+    return torch.cat([pool[p] for p in pages], dim=0).unsqueeze(0).contiguous()

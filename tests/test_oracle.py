@@ -353,3 +353,59 @@ def test_causal_split_combine_equals_unsplit(oracle_mod, bounds):
     o2, l2 = oracle_mod.split_attention(q, k, v, 0.6, bounds, causal=True)
     np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l2, lse, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- paged KV cache
+# The paged reference gathers each sequence's keys through its page table and
+# calls the pinned `attention`; these pins tie the gather to layouts whose
+# answer is known without it.
+def _paged_from_contiguous(k, v, page_size, perm_seed=None):
+    """Cut contiguous [b, sk, h, d] caches into pages of one pool (optionally
+    in a shuffled pool order) and return (k_pages, v_pages, table)."""
+    b, sk, h, d = k.shape
+    npg = sk // page_size
+    kp = k.reshape(b * npg, page_size, h, d)
+    vp = v.reshape(b * npg, page_size, h, d)
+    order = np.arange(b * npg)
+    if perm_seed is not None:
+        order = np.random.default_rng(perm_seed).permutation(b * npg)
+    # pool slot order[j] holds logical page j
+    kpool = np.empty_like(kp)
+    vpool = np.empty_like(vp)
+    kpool[order] = kp
+    vpool[order] = vp
+    table = order.reshape(b, npg)
+    return kpool, vpool, table
+
+
+@pytest.mark.parametrize("perm_seed", [None, 5])
+def test_paged_equals_contiguous_cache(oracle_mod, perm_seed):
+    b, sk, h, d, ps = 3, 12, 2, 4, 4
+    q, k, v = _rand((b, 1, h, d), 40), _rand((b, sk, h, d), 41), _rand((b, sk, h, d), 42)
+    kp, vp, table = _paged_from_contiguous(k, v, ps, perm_seed)
+    o, lse = oracle_mod.paged_attention(q, kp, vp, table, np.full(b, sk), 0.5)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, 0.5)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_paged_lengths_are_key_prefixes(oracle_mod):
+    b, sk, h, d, ps = 3, 12, 2, 4, 4
+    q, k, v = _rand((b, 1, h, d), 43), _rand((b, sk, h, d), 44), _rand((b, sk, h, d), 45)
+    kp, vp, table = _paged_from_contiguous(k, v, ps, 7)
+    lens = np.array([5, 12, 1])
+    o, lse = oracle_mod.paged_attention(q, kp, vp, table, lens, 0.8)
+    for i, n in enumerate(lens):
+        o_ref, lse_ref = oracle_mod.attention(q[i:i + 1], k[i:i + 1], v[i:i + 1], 0.8, key_range=(0, n))
+        np.testing.assert_allclose(o[i:i + 1], o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[i:i + 1], lse_ref, rtol=0, atol=1e-12)
+
+
+def test_paged_empty_sequence(oracle_mod):
+    b, sk, h, d, ps = 2, 8, 1, 3, 4
+    q, k, v = _rand((b, 1, h, d), 46), _rand((b, sk, h, d), 47), _rand((b, sk, h, d), 48)
+    kp, vp, table = _paged_from_contiguous(k, v, ps)
+    o, lse = oracle_mod.paged_attention(q, kp, vp, table, np.array([0, 8]), 1.0)
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    o_ref, lse_ref = oracle_mod.attention(q[1:], k[1:], v[1:], 1.0)
+    np.testing.assert_allclose(o[1:], o_ref, rtol=0, atol=1e-12)

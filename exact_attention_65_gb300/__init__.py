@@ -67,6 +67,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_splitkv_causal.restype = i32
         lib.attn_decode_splitkv_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                    f32, i32, i32, vp]
+        lib.attn_decode_paged.restype = i32
+        lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                          i32, f32, i32, i32, vp]
         lib.attn_decode_num_splits.restype = i32
         lib.attn_decode_num_splits.argtypes = [i32] * 5
         lib.attn_decode_num_splits_for_sms.restype = i32
@@ -172,6 +175,49 @@ def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0
                 b, sq, sk, h, d, scale, int(num_splits), dt, _stream(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_splitkv")
+    return out, lse
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float | None = None,
+                      num_splits: int = 0, out=None, lse=None, stream=None):
+    """Split-KV decode of one new row per sequence from a paged KV cache.
+
+    q: [b, 1, h, d]; k_pages, v_pages: [num_pages, page_size, h, d] (page_size
+    a multiple of 256); block_table: int32 [b, max_pages] pool page of each
+    logical page; seqlens_k: int32 [b] keys per sequence. All CUDA tensors."""
+    if not isinstance(q, torch.Tensor) or not q.is_cuda or q.dim() != 4 or q.shape[1] != 1:
+        raise ValueError("q must be a CUDA tensor [b, 1, h, d]")
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [num_pages, page_size, h, d]")
+        if t.dtype != q.dtype or t.device != q.device:
+            raise ValueError(f"{name} must match q's dtype and device")
+    if k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    for name, t in (("block_table", block_table), ("seqlens_k", seqlens_k)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda \
+                or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor on q's device")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    b, _, h, d = q.shape
+    num_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    if k_pages.shape[2] != h or k_pages.shape[3] != d:
+        raise ValueError("page pools must be [num_pages, page_size, h, d] with q's h and d")
+    if block_table.dim() != 2 or block_table.shape[0] != b or tuple(seqlens_k.shape) != (b,):
+        raise ValueError("block_table must be [b, max_pages] and seqlens_k [b]")
+    dt = _dtype_code(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, b, h, 1)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                   block_table.data_ptr(), seqlens_k.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), b, h, d, num_pages, page_size,
+                                   block_table.shape[1], scale, int(num_splits), dt,
+                                   _stream(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_paged")
     return out, lse
 
 

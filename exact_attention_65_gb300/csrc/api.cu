@@ -357,6 +357,75 @@ attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const voi
                    stream);
 }
 
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                                float *lse, int b, int h, int d, int num_pages, int page_size,
+                                int max_pages_per_seq, float scale, int num_splits,
+                                attn_dtype_t dtype, cudaStream_t stream) {
+    if (!block_table || !seqlens_k || !aligned(block_table, 4) || !aligned(seqlens_k, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (num_pages < 1 || page_size < 1 || max_pages_per_seq < 1 || num_splits < 0)
+        return ATTN_ERR_INVALID_ARG;
+    // a TMA box of the decode kernel (up to 256 key rows) never crosses a page
+    if (page_size % 256 != 0) return ATTN_ERR_UNSUPPORTED;
+    const int64_t sk_max = static_cast<int64_t>(max_pages_per_seq) * page_size;
+    if (sk_max > 0x7fffffffLL || static_cast<int64_t>(b) * max_pages_per_seq > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    // q [b, 1, h, d]; the pools stand in for k and v in the common checks
+    attn_status_t st = validate_args(q, k_pages, v_pages, o, lse, b, 1, static_cast<int>(sk_max),
+                                     h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    // The lengths live on the device: splits are chosen for the longest
+    // sequence the table allows; splits past a sequence's end are empty.
+    const int64_t nblocks = cdiv(sk_max, dec_block_rows(d));
+    int64_t splits = num_splits == 0
+                         ? dec_num_splits(b, 1, static_cast<int>(sk_max), h, d, ds->num_sms)
+                         : num_splits;
+    if (splits > nblocks) splits = nblocks;
+    if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
+    if (splits < 1) splits = 1;
+
+    CUtensorMap tk, tv;
+    if (!encode_4d(&tk, k_pages, bf16, d, h, page_size, num_pages, d, dec_box_rows(d),
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_4d(&tv, v_pages, bf16, d, h, page_size, num_pages, d, dec_box_rows(d),
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return ATTN_ERR_CUDA;
+    DecodeArgs a;
+    a.q = q;
+    a.o = o;
+    a.lse = lse;
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    a.b = b;
+    a.sq = 1;
+    a.sk = static_cast<int>(sk_max);
+    a.h = h;
+    a.splits = static_cast<int>(splits);
+    a.blocks_per_split = static_cast<int>(cdiv(nblocks, splits));
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = debug_flags();
+    a.block_table = block_table;
+    a.seqlens = seqlens_k;
+    a.page_size = page_size;
+    a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    if (splits == 1)
+        return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    void *ws = nullptr;
+    if ((st = alloc_partials(splits, b, 1, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
+        return st;
+    cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
+    if (e == cudaSuccess)
+        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, 1, h, a.splits, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                                   int b, int sq, int sk, int h, int d, float scale, int num_splits,
                                   cudaStream_t stream) {

@@ -205,6 +205,11 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
             const int r = warp * G::ROWS_PER_WARP + p * G::RPP + grp;
             float vf[8];
             unpack8<BF16>(*reinterpret_cast<const uint4 *>(vb + r * D * 2 + sub * 16), vf);
+            // Rows past the split's last key weigh 0; a paged cache's last page
+            // holds stale data there, which must not reach O even as 0 * NaN.
+            if (blk * G::BN + r >= row_end)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vf[e] = 0.f;
 #pragma unroll
             for (int qi = 0; qi < QR; ++qi)
 #pragma unroll
@@ -306,10 +311,13 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
     const int batch = blockIdx.z / nqb;
     const int q0 = (blockIdx.z % nqb) * QR;
     const int nq = min(QR, a.sq - q0);
-    const int nblocks = (a.sk + G::BN - 1) / G::BN;
+    // keys of this sequence: sk, or its own length with a paged cache
+    int sk_b = a.sk;
+    if (a.block_table) sk_b = min(max(a.seqlens[batch], 0), a.sk);
+    const int nblocks = (sk_b + G::BN - 1) / G::BN;
     const int blk0 = split * a.blocks_per_split;
     const int blk1 = min(nblocks, blk0 + a.blocks_per_split);
-    const int row_end = min(a.sk, blk1 * G::BN);
+    const int row_end = min(sk_b, blk1 * G::BN);
 
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC);
     if (threadIdx.x == 0) {
@@ -338,11 +346,21 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
                 const uint32_t dst = sbase + s * G::STAGE_BYTES;
 #pragma unroll
                 for (int x = 0; x < G::BOXES; ++x) {
-                    const int r = blk * G::BN + x * G::BOX_ROWS;
-                    tma_load_4d_hint(dst + x * G::BOX_ROWS * D * 2, &tk, full(s), 0, head, r, batch,
+                    int r = blk * G::BN + x * G::BOX_ROWS;
+                    int outer = batch;
+                    if (a.block_table) {
+                        // A box never crosses a page (page_size is a multiple of
+                        // 256). Rows past the sequence's end are masked by the
+                        // consumers; their page index is only kept in range.
+                        const int lp = min(r / a.page_size, a.max_pages - 1);
+                        const int pg = a.block_table[static_cast<int64_t>(batch) * a.max_pages + lp];
+                        outer = min(max(pg, 0), a.num_pages - 1);
+                        r -= lp * a.page_size;
+                    }
+                    tma_load_4d_hint(dst + x * G::BOX_ROWS * D * 2, &tk, full(s), 0, head, r, outer,
                                      stream_once);
                     tma_load_4d_hint(dst + G::BLOCK_BYTES + x * G::BOX_ROWS * D * 2, &tv, full(s), 0,
-                                     head, r, batch, stream_once);
+                                     head, r, outer, stream_once);
                 }
             }
             WaitGuard drain = g;

@@ -72,6 +72,16 @@ struct DecodeArgs {
     float scale_log2;
     uint32_t *status;
     uint32_t flags;
+    // Paged K/V (block_table != nullptr): the K/V maps cover page pools
+    // [num_pages, page_size, h, d]; key row r of sequence bb lives in page
+    // block_table[bb * max_pages + r / page_size] at row r % page_size, and
+    // the sequence has seqlens[bb] keys (sk above is then max_pages *
+    // page_size, the most it may have).
+    const int32_t *block_table = nullptr;
+    const int32_t *seqlens = nullptr;
+    int page_size = 0;
+    int max_pages = 0;
+    int num_pages = 0;
 };
 
 cudaError_t launch_decode(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,

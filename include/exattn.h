@@ -29,6 +29,8 @@
 #ifndef EXATTN_H
 #define EXATTN_H
 
+#include <stdint.h>
+
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -108,6 +110,35 @@ attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const voi
                                          float *lse, int b, int sq, int sk, int h, int d,
                                          float scale, int num_splits, attn_dtype_t dtype,
                                          cudaStream_t stream);
+
+/*
+ * Split-KV decode of one new query row per sequence from a paged KV cache.
+ * Paged caches are not on the pages beyond a mention ("Why FlashAttention is
+ * fast", section 5, item 2: FlashAttention with a paged KV cache is the
+ * standard for long contexts); the layout read here is the common one.
+ *   q            [b, 1, h, d] (device, 16-byte aligned)
+ *   k_pages,
+ *   v_pages      page pools [num_pages, page_size, h, d] (device, 16-byte
+ *                aligned); page_size must be a multiple of 256
+ *                (ATTN_ERR_UNSUPPORTED otherwise)
+ *   block_table  int32 [b, max_pages_per_seq] (device): logical page p of
+ *                sequence i is pool page block_table[i * max_pages_per_seq + p]
+ *   seqlens_k    int32 [b] (device): keys of sequence i, 0 <= seqlens_k[i]
+ *                <= max_pages_per_seq * page_size (values outside are
+ *                clamped; entries of the table past a sequence's last page
+ *                are not used)
+ *   o, lse       [b, 1, h, d] and fp32 [b, h, 1]
+ * The split count (num_splits = 0: the heuristic) is chosen for the longest
+ * allowed sequence, since the lengths are only known on the device; splits
+ * past a sequence's end are empty. A sequence with no key gets O = 0 and
+ * LSE = -inf. The reduce, the workspace and the errors are those of
+ * attn_decode_splitkv_ex.
+ */
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                                float *lse, int b, int h, int d, int num_pages, int page_size,
+                                int max_pages_per_seq, float scale, int num_splits,
+                                attn_dtype_t dtype, cudaStream_t stream);
 
 /*
  * Split-KV decode that allocates no device memory. The pages have no

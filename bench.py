@@ -410,6 +410,27 @@ def measure_extras(ea, dev, flush, stream, peaks):
             out[f"{name}/sq={sq}{tag}"] = {"ms": round(ms, 5), "GB/s (K+V)": round(gbs, 1),
                                            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
         del k, v, gen_q
+    # paged KV cache: the same decode problems with K/V in shuffled pages of
+    # 256 keys behind a block table
+    for name in ("decode_b8_h48_sk8192", "decode_b1_h16_sk32768"):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        ps = 256
+        npg = w.sk // ps
+        perm = torch.randperm(w.b * npg, generator=gen, device=dev)
+        kp = torch.empty((w.b * npg, ps, w.h, w.d), dtype=w.dtype, device=dev)
+        vp = torch.empty_like(kp)
+        kp[perm] = k.reshape(w.b * npg, ps, w.h, w.d)
+        vp[perm] = v.reshape(w.b * npg, ps, w.h, w.d)
+        table = perm.to(torch.int32).reshape(w.b, npg).contiguous()
+        lens = torch.full((w.b,), w.sk, dtype=torch.int32, device=dev)
+        del k, v
+        fn = lambda: ea.attn_decode_paged(q, kp, vp, table, lens, scale=w.scale)  # noqa: E731
+        (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+        gbs = w.io_bytes / (ms * 1e-3) / 1e9
+        out[f"{name}/paged256"] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
+                                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del q, kp, vp
     for name, split_list in (("decode_b8_h48_sk8192", [0]),
                              ("decode_b1_h16_sk32768", [0, 1, 2, 4, 8, 16])):
         w = workloads.WORKLOADS[name]

@@ -103,7 +103,7 @@ __device__ __forceinline__ bool consumer_sync_any(bool pred, int nthreads) {
     return r != 0;
 }
 
-template <int D, int QR, bool BF16, typename Full, typename Empty>
+template <int D, int QR, bool BF16, bool PAGED, typename Full, typename Empty>
 __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty empty, int warp,
                                                int lane, int split, int head, int batch, int q0,
                                                int nq, int blk0, int blk1, int row_end,
@@ -147,6 +147,7 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
         }
         const uint8_t *kb = smem + s * G::STAGE_BYTES;
         const uint8_t *vb = kb + G::BLOCK_BYTES;
+        const bool tail = PAGED && (blk + 1) * G::BN > row_end;
         float x[G::PASSES][QR];
 #pragma unroll
         for (int p = 0; p < G::PASSES; ++p) {
@@ -207,9 +208,13 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
             unpack8<BF16>(*reinterpret_cast<const uint4 *>(vb + r * D * 2 + sub * 16), vf);
             // Rows past the split's last key weigh 0; a paged cache's last page
             // holds stale data there, which must not reach O even as 0 * NaN.
-            if (blk * G::BN + r >= row_end)
+            // Only the split's last block can hold such rows. (A contiguous
+            // cache has TMA zero fill there.)
+            if constexpr (PAGED) {
+                if (tail && blk * G::BN + r >= row_end)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) vf[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) vf[e] = 0.f;
+            }
 #pragma unroll
             for (int qi = 0; qi < QR; ++qi)
 #pragma unroll
@@ -292,7 +297,7 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
     }
 }
 
-template <int D, int QR, bool BF16>
+template <int D, int QR, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(DecGeom<D>::THREADS)
     decode_split_kernel(const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const DecodeArgs a) {
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
     const int nq = min(QR, a.sq - q0);
     // keys of this sequence: sk, or its own length with a paged cache
     int sk_b = a.sk;
-    if (a.block_table) sk_b = min(max(a.seqlens[batch], 0), a.sk);
+    if constexpr (PAGED) sk_b = min(max(a.seqlens[batch], 0), a.sk);
     const int nblocks = (sk_b + G::BN - 1) / G::BN;
     const int blk0 = split * a.blocks_per_split;
     const int blk1 = min(nblocks, blk0 + a.blocks_per_split);
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
                 for (int x = 0; x < G::BOXES; ++x) {
                     int r = blk * G::BN + x * G::BOX_ROWS;
                     int outer = batch;
-                    if (a.block_table) {
+                    if constexpr (PAGED) {
                         // A box never crosses a page (page_size is a multiple of
                         // 256). Rows past the sequence's end are masked by the
                         // consumers; their page index is only kept in range.
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
                 mbar_wait(full(i % G::STAGES), (i / G::STAGES) & 1, drain, 2);
         }
     } else {
-        decode_consume<D, QR, BF16>(smem, full, empty, warp, lane, split, head, batch, q0, nq, blk0,
+        decode_consume<D, QR, BF16, PAGED>(smem, full, empty, warp, lane, split, head, batch, q0, nq, blk0,
                                     blk1, row_end, a, g);
     }
     __syncthreads();
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) lse[lse_idx] = L;
 }
 
-template <int D, int QR, bool BF16>
+template <int D, int QR, bool BF16, bool PAGED>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                             cudaStream_t stream) {
     using G = DecGeom<D>;
@@ -452,22 +457,23 @@ cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<D, QR, BF16>,
+        e = cudaFuncSetAttribute(decode_split_kernel<D, QR, BF16, PAGED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const int nqb = (a.sq + QR - 1) / QR;
     dim3 grid(a.splits, a.h, a.b * nqb);
-    decode_split_kernel<D, QR, BF16><<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(tk, tv, a);
+    decode_split_kernel<D, QR, BF16, PAGED><<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
 template <int D, bool BF16>
 cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                             cudaStream_t stream) {
-    if (a.sq == 1) return launch_decode_t<D, 1, BF16>(tk, tv, a, stream);
-    return launch_decode_t<D, 4, BF16>(tk, tv, a, stream);
+    if (a.block_table) return launch_decode_t<D, 1, BF16, true>(tk, tv, a, stream);  // sq == 1
+    if (a.sq == 1) return launch_decode_t<D, 1, BF16, false>(tk, tv, a, stream);
+    return launch_decode_t<D, 4, BF16, false>(tk, tv, a, stream);
 }
 
 template <int D, bool BF16>

@@ -215,3 +215,53 @@ def _stack_pages(pool, pages):
     import torch
 
     return torch.cat([pool[p] for p in pages], dim=0).unsqueeze(0).contiguous()
+
+
+def _f64(x):
+    """fp64 copy of a host tensor or array (16-bit values widen exactly)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(x, torch.Tensor):
+        if x.is_cuda:
+            raise ValueError("the oracle takes host tensors only")
+        return x.to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def attention_backward(q, k, v, do, scale: float, causal=False):
+    """Gradients of the exact attention of ``attention``, by the chain rule of
+    its plain definition (the flash-attn timing issue times a backward pass;
+    none of the pages writes one out). With S = scale * Q K^T, P = softmax(S)
+    row by row, O = P V and the upstream gradient dO:
+        dV = P^T dO,   dP = dO V^T,   D = rowsum(P * dP),   dS = P * (dP - D),
+        dQ = scale * dS K,   dK = scale * dS^T Q.
+    With ``causal`` the masked scores of ``attention`` (bottom-right aligned)
+    have P = 0; a row that sees no key has P = 0 throughout.
+
+    q, do: [b, sq, h, d]; k, v: [b, sk, h, d] (host tensors or arrays).
+    Returns (dq, dk, dv) as fp64 numpy arrays of the input shapes."""
+    Q, K, V, dO = (_f64(t) for t in (q, k, v, do))
+    b, sq, h, d = Q.shape
+    sk = K.shape[1]
+    dq, dk, dv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    visible = np.ones((sq, sk), dtype=bool)
+    if causal:
+        visible = np.arange(sk)[None, :] <= np.arange(sq)[:, None] + (sk - sq)
+    for bb in range(b):
+        for hh in range(h):
+            Qh, Kh, Vh, dOh = Q[bb, :, hh], K[bb, :, hh], V[bb, :, hh], dO[bb, :, hh]
+            S = np.where(visible, scale * (Qh @ Kh.T), -np.inf)
+            P = np.zeros_like(S)
+            seen = visible.any(axis=1)
+            Ss = S[seen]
+            E = np.exp(Ss - Ss.max(axis=1, keepdims=True))
+            P[seen] = E / E.sum(axis=1, keepdims=True)
+            dP = dOh @ Vh.T
+            D = (P * dP).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            dq[bb, :, hh] = scale * (dS @ Kh)
+            dk[bb, :, hh] = scale * (dS.T @ Qh)
+            dv[bb, :, hh] = P.T @ dOh
+    return dq, dk, dv

@@ -409,3 +409,58 @@ def test_paged_empty_sequence(oracle_mod):
     assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
     o_ref, lse_ref = oracle_mod.attention(q[1:], k[1:], v[1:], 1.0)
     np.testing.assert_allclose(o[1:], o_ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward pass
+# The gradients by the chain rule; pinned to torch's fp64 autograd (a library
+# special case), to finite differences of the oracle's own forward, and to
+# identities that hold for any input.
+def _loss_grads_torch(q, k, v, do, scale, causal):
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2).requires_grad_(True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale, is_causal=causal)
+    o.backward(torch.from_numpy(do).transpose(1, 2))
+    return tuple(t.grad.transpose(1, 2).numpy() for t in (tq, tk, tv))
+
+
+@pytest.mark.parametrize("shape,scale,causal", [((2, 7, 11, 3, 5), 0.45, False),
+                                                ((1, 9, 9, 2, 4), 0.8, True),
+                                                ((1, 1, 6, 2, 3), -0.6, False)])
+def test_backward_is_torch_autograd(oracle_mod, shape, scale, causal):
+    b, sq, sk, h, d = shape
+    q, k, v = _rand((b, sq, h, d), 50), _rand((b, sk, h, d), 51), _rand((b, sk, h, d), 52)
+    do = _rand((b, sq, h, d), 53)
+    dq, dk, dv = oracle_mod.attention_backward(q, k, v, do, scale, causal=causal)
+    rq, rk, rv = _loss_grads_torch(q, k, v, do, scale, causal)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_backward_finite_differences(oracle_mod, which):
+    """<grad, E> equals the central difference of L = sum(O * G) along E."""
+    b, sq, sk, h, d, scale = 1, 3, 4, 1, 2, 0.7
+    x = [_rand((b, sq, h, d), 54), _rand((b, sk, h, d), 55), _rand((b, sk, h, d), 56)]
+    G = _rand((b, sq, h, d), 57)
+    E = _rand(x[which].shape, 58)
+    grads = oracle_mod.attention_backward(x[0], x[1], x[2], G, scale)
+    eps = 1e-5
+
+    def loss(t):
+        y = list(x)
+        y[which] = x[which] + t * E
+        o, _ = oracle_mod.attention(y[0], y[1], y[2], scale)
+        return float((o * G).sum())
+
+    fd = (loss(eps) - loss(-eps)) / (2 * eps)
+    assert abs(float((grads[which] * E).sum()) - fd) < 1e-8
+
+
+def test_backward_identities(oracle_mod):
+    """dS rows sum to 0, so dK sums to 0 over the keys; every column of P
+    sums the upstream gradient into dV: sum_j dV_j = sum_i dO_i."""
+    b, sq, sk, h, d = 2, 6, 9, 2, 4
+    q, k, v = _rand((b, sq, h, d), 59), _rand((b, sk, h, d), 60), _rand((b, sk, h, d), 61)
+    do = _rand((b, sq, h, d), 62)
+    dq, dk, dv = oracle_mod.attention_backward(q, k, v, do, 0.5)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), atol=1e-12)

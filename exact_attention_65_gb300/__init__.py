@@ -70,6 +70,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_paged.restype = i32
         lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                           i32, f32, i32, i32, vp]
+        lib.attn_bwd.restype = i32
+        lib.attn_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, i32, vp]
         lib.attn_decode_num_splits.restype = i32
         lib.attn_decode_num_splits.argtypes = [i32] * 5
         lib.attn_decode_num_splits_for_sms.restype = i32
@@ -219,6 +221,37 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float 
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None, dv=None,
+             stream=None):
+    """Backward pass of attn_fwd (non-causal): returns (dq, dk, dv).
+
+    q, o, dout: [b, sq, h, d]; k, v: [b, sk, h, d] (fp16 or bf16, contiguous
+    CUDA tensors); lse: fp32 [b, h, sq] from attn_fwd."""
+    b, sq, sk, h, d, dt = _check(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != q.dtype \
+                or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous tensor like q")
+    if (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
+            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 tensor [b, h, sq]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous tensor like {name[1]}")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode_num_splits(b: int, sq: int, sk: int, h: int, d: int) -> int:

@@ -256,6 +256,56 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
                    stream);
 }
 
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv, int b,
+                       int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    if (!dout || !dq || !dk || !dv || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) ||
+        !aligned(dv, 16))
+        return ATTN_ERR_INVALID_ARG;
+    if (cdiv(sq, 128) * h * b > 0x7fffffffLL || cdiv(sk, 128) * h * b > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    const int box0 = fwd_row_bytes(d) / 2;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, 128, fwd_swizzle(d)) ||
+        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, 128, fwd_swizzle(d)) ||
+        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, 128, fwd_swizzle(d)) ||
+        !encode_4d(&tdo, dout, bf16, d, h, sq, b, box0, 128, fwd_swizzle(d)))
+        return ATTN_ERR_CUDA;
+    BwdArgs a;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.b = b;
+    a.sq = sq;
+    a.sk = sk;
+    a.h = h;
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = debug_flags();
+    a.num_sms = ds->num_sms;
+    // D = rowsum(dO * O), fp32 [b, h, sq], from the stream-ordered pool
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, static_cast<size_t>(b) * h * sq * sizeof(float), stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_MEMORY;
+    }
+    a.dvec = static_cast<float *>(ws);
+    const cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms) {
     if (sq == 1) return dec_num_splits(b, sq, sk, h, d, num_sms);
     if (b < 1 || sq < 1 || sk < 1 || h < 1 || num_sms < 1) return 0;

@@ -1,0 +1,545 @@
+// Backward pass of exact attention on sm_103a: dQ, dK, dV from Q, K, V, the
+// forward's O and LSE, and the upstream gradient dO.
+//
+// The pages time a backward pass (the flash-attn timing issue) but do not
+// write one out; what is computed is the chain rule of the forward's
+// definition. With S = scale * Q K^T, P = softmax(S) by rows (recomputed
+// from the saved LSE: P = exp(S - LSE)), O = P V:
+//     dV = P^T dO,   dP = dO V^T,   D = rowsum(dO * O) = rowsum(P * dP),
+//     dS = P * (dP - D),   dQ = scale * dS K,   dK = scale * dS^T Q.
+// Nothing of size s^2 goes to HBM: each score tile is recomputed on chip,
+// as in the forward ("Why FlashAttention is fast", section 3.2).
+//
+// Three kernels:
+//   bwd_dot_kernel   D = rowsum(dO * O), fp32 [b, h, sq].
+//   bwd_kernel<DQ>   one unit = a 128-row query tile; it keeps Q and dO in
+//                    shared memory, streams K_j and V_j, and accumulates
+//                    dQ += dS K_j in TMEM.
+//   bwd_kernel<DKV>  one unit = a 128-key tile; it keeps K and V, streams
+//                    Q_i and dO_i, and accumulates dV += P^T dO_i and
+//                    dK += dS^T Q_i in TMEM.
+// Computing dQ in its own pass (recomputing S and dP once more) avoids
+// accumulating it across CTAs with atomics.
+//
+// Both are persistent kernels with the forward's roles: warp 0 is the TMA
+// producer (the unit's fixed pair of tiles, then a ring of streamed tiles),
+// one thread of warp 1 issues the tcgen05 MMAs, warps 4-7 hold one TMEM lane
+// (one row of the tile) per thread and do the elementwise work. For each
+// step the MMAs write the score tile and the dP tile to TMEM; the warps turn
+// them into 16-bit P and dS written back in place; then the accumulating
+// MMAs read them from TMEM.
+//
+// TMEM columns: [0, 128) score tile (then P or dS), [128, 256) dP tile (then
+// dS in the dK/dV kernel), [256, 256 + d) dQ or dV, [384, 384 + d) dK.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace exattn {
+namespace {
+
+constexpr int kBwdDQ = 0;   // query-tile units: dQ
+constexpr int kBwdDKV = 1;  // key-tile units: dK and dV
+// warp 0 producer, warp 1 MMA issuer, warps 2-3 idle, warps 4-7 elementwise
+constexpr int kBwdThreads = 256;
+
+template <int D>
+struct BwdGeom {
+    static constexpr int BT = 128;  // rows of every tile
+    static constexpr int ROW_BYTES = fwd_row_bytes(D);
+    static constexpr int PANELS = (D * 2) / ROW_BYTES;
+    static constexpr int PANEL_ELEMS = ROW_BYTES / 2;
+    static constexpr int PANEL_BYTES = BT * ROW_BYTES;
+    static constexpr int TILE_BYTES = BT * D * 2;
+    static constexpr int SLOTS = D == 128 ? 4 : 8;  // streamed tiles, two per step
+    static constexpr uint32_t LAYOUT =
+        ROW_BYTES == 128 ? kLayoutSw128 : (ROW_BYTES == 64 ? kLayoutSw64 : kLayoutSw32);
+    static constexpr uint32_t SBO = 8 * ROW_BYTES;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int T_S = 0, T_P = 128, T_A0 = 256, T_A1 = 384;
+
+    static constexpr int OFF_FIX = 0;                       // the unit's two fixed tiles
+    static constexpr int OFF_RING = 2 * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + SLOTS * TILE_BYTES;
+    // barriers: fix_full | fix_empty | ring_full[SLOTS] | ring_empty[SLOTS] |
+    //           s_full | p_full | acc_full | acc_empty | done
+    static constexpr int BAR_FF = 0;
+    static constexpr int BAR_FE = 1;
+    static constexpr int BAR_RF = 2;
+    static constexpr int BAR_RE = BAR_RF + SLOTS;
+    static constexpr int BAR_SF = BAR_RE + SLOTS;
+    static constexpr int BAR_PF = BAR_SF + 1;
+    static constexpr int BAR_AF = BAR_PF + 1;
+    static constexpr int BAR_AE = BAR_AF + 1;
+    static constexpr int BAR_DONE = BAR_AE + 1;
+    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int USED = OFF_MISC + 16;
+    static constexpr int MIN_SMEM = 120 * 1024;  // one CTA per SM: it owns all of TMEM
+    static constexpr int SMEM_BYTES = (USED > MIN_SMEM ? USED : MIN_SMEM) + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2b(float lo, float hi) {
+    if constexpr (BF16)
+        return cvt_pack_bf16(lo, hi);
+    else
+        return cvt_pack_f16(lo, hi);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float to_f32(uint16_t bits) {
+    if constexpr (BF16)
+        return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    else
+        return __half2float(__ushort_as_half(bits));
+}
+
+// D[b, h, i] = sum_t dO[b, i, h, t] * O[b, i, h, t] in fp32; d/8 lanes per row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    bwd_dot_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ dout,
+                   float *__restrict__ dvec, int b, int sq, int h) {
+    constexpr int LPR = D / 8;
+    constexpr int RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = static_cast<int64_t>(b) * sq * h;
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5)) *
+                          RPW + lane / LPR;
+    const int sub = lane % LPR;
+    float acc = 0.f;
+    if (r < rows) {
+        const uint4 wo = *reinterpret_cast<const uint4 *>(o + r * D + sub * 8);
+        const uint4 wd = *reinterpret_cast<const uint4 *>(dout + r * D + sub * 8);
+        const uint32_t uo[4] = {wo.x, wo.y, wo.z, wo.w};
+        const uint32_t ud[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(to_f32<BF16>(static_cast<uint16_t>(uo[i] & 0xffffu)),
+                       to_f32<BF16>(static_cast<uint16_t>(ud[i] & 0xffffu)), acc);
+            acc = fmaf(to_f32<BF16>(static_cast<uint16_t>(uo[i] >> 16)),
+                       to_f32<BF16>(static_cast<uint16_t>(ud[i] >> 16)), acc);
+        }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (r < rows && sub == 0) {
+        // r = (batch * sq + i) * h + head  ->  [b, h, sq]
+        const int head = static_cast<int>(r % h);
+        const int64_t bi = r / h;
+        const int i = static_cast<int>(bi % sq);
+        const int64_t batch = bi / sq;
+        dvec[(batch * h + head) * sq + i] = acc;
+    }
+}
+
+// A unit: tile `tile` (128 rows) of one (batch, head); its rows are query
+// rows (dQ kernel) or key rows (dK/dV kernel).
+struct BUnit {
+    int tile, head, batch;
+};
+
+__device__ __forceinline__ BUnit bunit_of(int u, int ntiles, int h) {
+    BUnit x;
+    x.tile = u % ntiles;
+    const int r = u / ntiles;
+    x.head = r % h;
+    x.batch = r / h;
+    return x;
+}
+
+template <int D, int MODE>
+__device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
+                                             const CUtensorMap *tv, const CUtensorMap *tdo,
+                                             uint32_t sbase, int ntiles, int nsteps, int units,
+                                             int h, const WaitGuard &g) {
+    using G = BwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    // the unit's fixed pair and the streamed pair of each step
+    const CUtensorMap *fa = MODE == kBwdDQ ? tq : tk;
+    const CUtensorMap *fb = MODE == kBwdDQ ? tdo : tv;
+    const CUtensorMap *sa = MODE == kBwdDQ ? tk : tq;
+    const CUtensorMap *sb = MODE == kBwdDQ ? tv : tdo;
+    const uint64_t keep = policy_evict_last();  // streamed tiles are re-read by other units
+    int it_u = 0, n_issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
+        const BUnit x = bunit_of(u, ntiles, h);
+        if (!mbar_wait(bar(G::BAR_FE), (it_u & 1) ^ 1, g, 1)) break;
+        mbar_arrive_expect_tx(bar(G::BAR_FF), 2 * G::TILE_BYTES);
+        for (int p = 0; p < G::PANELS; ++p) {
+            tma_load_4d(sbase + G::OFF_FIX + p * G::PANEL_BYTES, fa, bar(G::BAR_FF),
+                        p * G::PANEL_ELEMS, x.head, x.tile * G::BT, x.batch);
+            tma_load_4d(sbase + G::OFF_FIX + G::TILE_BYTES + p * G::PANEL_BYTES, fb, bar(G::BAR_FF),
+                        p * G::PANEL_ELEMS, x.head, x.tile * G::BT, x.batch);
+        }
+        for (int i = 0; i < 2 * nsteps; ++i) {  // step j: item 2j from sa, 2j + 1 from sb
+            const int s = n_issued % G::SLOTS;
+            if (!mbar_wait(bar(G::BAR_RE + s), ((n_issued / G::SLOTS) & 1) ^ 1, g, 2)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(bar(G::BAR_RF + s), G::TILE_BYTES);
+            const CUtensorMap *map = (i & 1) ? sb : sa;
+            for (int p = 0; p < G::PANELS; ++p)
+                tma_load_4d_hint(sbase + G::OFF_RING + s * G::TILE_BYTES + p * G::PANEL_BYTES, map,
+                                 bar(G::BAR_RF + s), p * G::PANEL_ELEMS, x.head, (i >> 1) * G::BT,
+                                 x.batch, keep);
+            ++n_issued;
+        }
+    }
+    // wait (bounded, even after an abort) for the copies still landing
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    if (it_u > 0) mbar_wait(bar(G::BAR_FF), (it_u - 1) & 1, drain, 9);
+    for (int n = (n_issued > G::SLOTS ? n_issued - G::SLOTS : 0); n < n_issued; ++n)
+        mbar_wait(bar(G::BAR_RF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
+}
+
+template <int D, int MODE, bool BF16>
+__device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int nsteps, int units,
+                                        const WaitGuard &g) {
+    using G = BwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    constexpr uint32_t idesc_sq = mma_idesc_f16(G::BT, G::BT, BF16, false, false);  // 128x128 tiles
+    constexpr uint32_t idesc_acc = mma_idesc_f16(G::BT, D, BF16, false, true);      // ... x d, B MN-major
+    // K-major and MN-major descriptors of the fixed tiles and of ring slot 0
+    const uint64_t fix_k = smem_desc(sbase + G::OFF_FIX, 16, G::SBO, G::LAYOUT);
+    const uint64_t ring_k = smem_desc(sbase + G::OFF_RING, 16, G::SBO, G::LAYOUT);
+    const uint64_t ring_mn = smem_desc(sbase + G::OFF_RING, G::PANEL_BYTES, G::SBO, G::LAYOUT);
+    constexpr uint32_t tile16 = G::TILE_BYTES >> 4;
+
+    // A (K-major, fixed or ring) times B (K-major) over the head dim: a 128 x 128 tile.
+    auto mma_kk = [&](uint32_t dst, uint64_t adesc, uint64_t bdesc) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int p = (kk * 16) / G::PANEL_ELEMS;
+            const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
+            const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
+            mma_ss(dst, adesc + o16, bdesc + o16, idesc_sq, kk > 0 ? 1u : 0u);
+        }
+    };
+    // acc (+)= A[TMEM, 128 rows x 128] * B[128 x d, MN-major], 16 rows of B per MMA
+    auto mma_acc = [&](uint32_t dst, uint32_t a_tmem, uint64_t bdesc_mn, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < G::BT / 16; ++kk)
+            mma_ts(dst, a_tmem + kk * 8, bdesc_mn + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_acc,
+                   (!first || kk > 0) ? 1u : 0u);
+    };
+
+    int it_u = 0, base = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
+        if (!mbar_wait(bar(G::BAR_FF), it_u & 1, g, 4)) break;
+        for (int j = 0; j < nsteps; ++j) {
+            const int na = 2 * (base + j), nb = na + 1;
+            const int sa = na % G::SLOTS, sb = nb % G::SLOTS;
+            if (!mbar_wait(bar(G::BAR_RF + sa), (na / G::SLOTS) & 1, g, 5) ||
+                !mbar_wait(bar(G::BAR_RF + sb), (nb / G::SLOTS) & 1, g, 6)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if constexpr (MODE == kBwdDQ) {
+                // S = Q K_j^T, dP = dO V_j^T
+                mma_kk(tmem + G::T_S, fix_k, ring_k + sa * tile16);
+                mma_kk(tmem + G::T_P, fix_k + tile16, ring_k + sb * tile16);
+            } else {
+                // S^T = K Q_i^T, dP^T = V dO_i^T
+                mma_kk(tmem + G::T_S, fix_k, ring_k + sa * tile16);
+                mma_kk(tmem + G::T_P, fix_k + tile16, ring_k + sb * tile16);
+            }
+            mma_commit(bar(G::BAR_SF));
+            // the warps turn the tiles into 16-bit P / dS in place
+            if (!mbar_wait(bar(G::BAR_PF), (base + j) & 1, g, 8)) {
+                ok = false;
+                break;
+            }
+            // The first accumulation of a unit overwrites the accumulators: the
+            // previous unit's epilogue must have read them out.
+            if (j == 0 && !mbar_wait(bar(G::BAR_AE), (it_u & 1) ^ 1, g, 7)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if constexpr (MODE == kBwdDQ) {
+                mma_acc(tmem + G::T_A0, tmem + G::T_S, ring_mn + sa * tile16, j == 0);  // dQ += dS K_j
+            } else {
+                mma_acc(tmem + G::T_A0, tmem + G::T_S, ring_mn + sb * tile16, j == 0);  // dV += P^T dO_i
+                mma_acc(tmem + G::T_A1, tmem + G::T_P, ring_mn + sa * tile16, j == 0);  // dK += dS^T Q_i
+            }
+            mma_commit(bar(G::BAR_RE + sa));
+            mma_commit(bar(G::BAR_RE + sb));
+            if (j == nsteps - 1) {
+                mma_commit(bar(G::BAR_FE));
+                mma_commit(bar(G::BAR_AF));
+            }
+        }
+        base += nsteps;
+    }
+    mma_commit(bar(G::BAR_DONE));
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
+}
+
+// Store `cols` columns (multiple of 16) of one fp32 TMEM row, scaled, as
+// 16-bit values at dst.
+template <int COLS, bool BF16>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *dst, bool out) {
+#pragma unroll
+    for (int c0 = 0; c0 < COLS; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c0, v);
+        tmem_wait_ld();
+        if (out) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                pk[i] = pack2b<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    }
+}
+
+template <int D, int MODE, bool BF16>
+__device__ __forceinline__ void bwd_compute(uint32_t sbase, uint32_t tmem, int q4, int ntiles,
+                                            int nsteps, int units, const BwdArgs &a,
+                                            const WaitGuard &g) {
+    using G = BwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    const uint32_t lane = threadIdx.x & 31;
+    const int row = q4 * 32 + lane;  // TMEM lane = row of the unit's tile
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    const float c = a.scale_log2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    int it_u = 0, step = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it_u) {
+        const BUnit x = bunit_of(u, ntiles, a.h);
+        const int grow = x.tile * G::BT + row;
+        const int64_t bh = static_cast<int64_t>(x.batch) * a.h + x.head;
+        // dQ kernel: this row's LSE (log2 units) and D; rows past sq take no part
+        float lse2 = INFINITY, drow = 0.f;
+        if constexpr (MODE == kBwdDQ) {
+            if (grow < a.sq) {
+                lse2 = a.lse[bh * a.sq + grow] * kLog2e;
+                drow = a.dvec[bh * a.sq + grow];
+            }
+        }
+        for (int j = 0; j < nsteps; ++j, ++step) {
+            const bool ok = mbar_wait(bar(G::BAR_SF), step & 1, g, 13);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            if constexpr (MODE == kBwdDQ) {
+                // row = query row; columns = keys j*128 .. : P = 2^(s c - lse2),
+                // dS = P (dP - D); keys past sk (TMA zero fill) take no part.
+                const int kv = a.sk - j * G::BT;
+#pragma unroll
+                for (int c0 = 0; c0 < G::BT; c0 += 32) {
+                    uint32_t sv[32], pv[32];
+                    tmem_ld32(tmem + lanes + G::T_S + c0, sv);
+                    tmem_ld32(tmem + lanes + G::T_P + c0, pv);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int k = c0 + 2 * i;
+                        const float p0 = k < kv ? fast_exp2(__uint_as_float(sv[2 * i]) * c - lse2) : 0.f;
+                        const float p1 =
+                            k + 1 < kv ? fast_exp2(__uint_as_float(sv[2 * i + 1]) * c - lse2) : 0.f;
+                        pk[i] = pack2b<BF16>(p0 * (__uint_as_float(pv[2 * i]) - drow),
+                                             p1 * (__uint_as_float(pv[2 * i + 1]) - drow));
+                    }
+                    // dS of keys c0 .. c0+31 into columns c0/2 .. c0/2+15, all read already
+                    tmem_st16(tmem + lanes + G::T_S + c0 / 2, pk);
+                }
+            } else {
+                // row = key row; columns = query rows j*128 .. with their own
+                // LSE and D (loads of one address across the warp); query rows
+                // past sq take no part.
+                const int nq = a.sq - j * G::BT;
+                const float *lse_j = a.lse + bh * a.sq + j * G::BT;
+                const float *d_j = a.dvec + bh * a.sq + j * G::BT;
+#pragma unroll
+                for (int c0 = 0; c0 < G::BT; c0 += 16) {
+                    uint32_t sv[16], pv[16];
+                    tmem_ld16(tmem + lanes + G::T_S + c0, sv);
+                    tmem_ld16(tmem + lanes + G::T_P + c0, pv);
+                    tmem_wait_ld();
+                    uint32_t pp[8], pd[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float pr[2], dr[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int col = c0 + 2 * i + e;
+                            const bool in = col < nq;
+                            const float l2 = in ? __ldg(lse_j + col) * kLog2e : INFINITY;
+                            const float dd = in ? __ldg(d_j + col) : 0.f;
+                            const float p = in ? fast_exp2(__uint_as_float(sv[2 * i + e]) * c - l2) : 0.f;
+                            pr[e] = p;
+                            dr[e] = p * (__uint_as_float(pv[2 * i + e]) - dd);
+                        }
+                        pp[i] = pack2b<BF16>(pr[0], pr[1]);
+                        pd[i] = pack2b<BF16>(dr[0], dr[1]);
+                    }
+                    // P^T and dS^T of columns c0 .. c0+15 into columns c0/2 .. c0/2+7
+                    tmem_st8(tmem + lanes + G::T_S + c0 / 2, pp);
+                    tmem_st8(tmem + lanes + G::T_P + c0 / 2, pd);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(G::BAR_PF));
+        }
+
+        // ---------------------------------------------------- epilogue
+        const bool ok = mbar_wait(bar(G::BAR_AF), it_u & 1, g, 14);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        const float scale = a.scale;
+        if constexpr (MODE == kBwdDQ) {
+            const bool out = grow < a.sq;
+            uint16_t *dst = reinterpret_cast<uint16_t *>(a.dq) +
+                            ((static_cast<int64_t>(x.batch) * a.sq + (out ? grow : 0)) * a.h + x.head) * D;
+            store_row<D, BF16>(tmem + lanes + G::T_A0, scale, dst, out);
+        } else {
+            const bool out = grow < a.sk;
+            const int64_t off =
+                ((static_cast<int64_t>(x.batch) * a.sk + (out ? grow : 0)) * a.h + x.head) * D;
+            store_row<D, BF16>(tmem + lanes + G::T_A0, 1.0f, reinterpret_cast<uint16_t *>(a.dv) + off, out);
+            store_row<D, BF16>(tmem + lanes + G::T_A1, scale, reinterpret_cast<uint16_t *>(a.dk) + off,
+                               out);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(G::BAR_AE));
+    }
+}
+
+template <int D, int MODE, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+               const BwdArgs a) {
+    using G = BwdGeom<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const int nq_t = (a.sq + G::BT - 1) / G::BT;
+    const int nk_t = (a.sk + G::BT - 1) / G::BT;
+    const int ntiles = MODE == kBwdDQ ? nq_t : nk_t;   // tiles that make units
+    const int nsteps = MODE == kBwdDQ ? nk_t : nq_t;   // streamed tiles per unit
+    const int units = ntiles * a.h * a.b;
+
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + G::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < G::NUM_BARS; ++i)
+            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_AE) ? 4u : 1u);  // one per compute warp
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitGuard g{abort_flag, a.status, kKernBwd};
+
+    if (warp == 0) {
+        if (lane == 0 && !(a.flags & kFlagSkipLoads)) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tdo);
+            bwd_producer<D, MODE>(&tq, &tk, &tv, &tdo, sbase, ntiles, nsteps, units, a.h, g);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) bwd_mma<D, MODE, BF16>(sbase, tmem, nsteps, units, g);
+    } else if (warp >= 4 && warp < 8) {
+        bwd_compute<D, MODE, BF16>(sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
+}
+
+template <int D, int MODE, bool BF16>
+cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
+    using G = BwdGeom<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(bwd_kernel<D, MODE, BF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int64_t ntiles = MODE == kBwdDQ ? (a.sq + G::BT - 1) / G::BT : (a.sk + G::BT - 1) / G::BT;
+    const int64_t units = ntiles * a.h * a.b;
+    const int64_t ctas = units < a.num_sms ? units : a.num_sms;
+    bwd_kernel<D, MODE, BF16>
+        <<<static_cast<unsigned>(ctas), kBwdThreads, G::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
+    // D = rowsum(dO * O), then dK/dV, then dQ
+    constexpr int RPW = 32 / (D / 8);
+    const int64_t rows = static_cast<int64_t>(a.b) * a.sq * a.h;
+    const int64_t warps = (rows + RPW - 1) / RPW;
+    bwd_dot_kernel<D, BF16><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.dvec, a.b,
+        a.sq, a.h);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_bwd_t<D, kBwdDKV, BF16>(tq, tk, tv, tdo, a, stream);
+    if (e != cudaSuccess) return e;
+    return launch_bwd_t<D, kBwdDQ, BF16>(tq, tk, tv, tdo, a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,
+                       cudaStream_t stream) {
+#define EXATTN_BWD_CASE(DD)                                                \
+    case DD:                                                               \
+        return bf16 ? launch_bwd_d<DD, true>(tq, tk, tv, tdo, a, stream)   \
+                    : launch_bwd_d<DD, false>(tq, tk, tv, tdo, a, stream);
+    switch (d) {
+        EXATTN_BWD_CASE(16)
+        EXATTN_BWD_CASE(32)
+        EXATTN_BWD_CASE(64)
+        EXATTN_BWD_CASE(128)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef EXATTN_BWD_CASE
+}
+
+}  // namespace exattn

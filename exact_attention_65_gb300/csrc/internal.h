@@ -46,6 +46,25 @@ struct FwdArgs {
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdArgs &a, cudaStream_t stream);
 
+// ------------------------------------------------------------ backward
+struct BwdArgs {
+    const void *o;      // forward output [b, sq, h, d]
+    const void *dout;   // upstream gradient [b, sq, h, d]
+    const float *lse;   // forward LSE [b, h, sq] (natural log)
+    float *dvec;        // workspace: D = rowsum(dO * O) [b, h, sq]
+    void *dq, *dk, *dv;
+    int b, sq, sk, h;
+    float scale;
+    float scale_log2;  // scale * log2(e)
+    uint32_t *status;
+    uint32_t flags;
+    int num_sms;
+};
+
+cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,
+                       cudaStream_t stream);
+
 // ------------------------------------------------------------ decode
 // Keys are streamed in blocks of 16 KB per tensor (dec_block_rows(d) rows).
 constexpr int DEC_BLOCK_BYTES = 16384;

@@ -74,6 +74,25 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
                               attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * Backward pass of attn_fwd (non-causal): dq, dk, dv from q, k, v, the
+ * forward's o and lse, and the upstream gradient dout. The flash-attn timing
+ * issue times a backward pass; none of the pages writes one out, so it is
+ * the chain rule of the forward's definition: with P = exp(scale Q K^T - LSE),
+ *     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, o, dout, dq   [b, sq, h, d]; k, v, dk, dv [b, sk, h, d]; lse fp32
+ *                    [b, h, sq] as written by attn_fwd; all in `dtype`
+ *                    except lse, device pointers, 16-byte aligned.
+ * Every output element is written. A workspace of 4 * b * h * sq bytes is
+ * taken stream-ordered from the device's default memory pool and returned.
+ * Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be had.
+ */
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                       int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                       cudaStream_t stream);
+
+/*
  * Split-KV decode, bf16 q/k/v/o ("where is flash decoding second stage
  * (reduce) code?" issue). seqlen_k is cut into num_splits ranges of whole
  * key blocks; split i writes its own O_i and LSE_i (fp32, library

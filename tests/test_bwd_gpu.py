@@ -1,0 +1,62 @@
+"""Backward-pass parity: attn_bwd (through the C ABI) against the fp64
+oracle's chain-rule gradients.
+
+The forward runs on the GPU (its O and LSE feed the backward, as in use);
+the oracle recomputes everything from the same rounded inputs in fp64.
+Shapes: single tiles, ragged query and key tails, sq != sk, several units
+per CTA, every head dim and both dtypes.
+
+Tolerance. The gradients are sums over keys (dQ) or query rows (dK, dV) of
+products that go through 16-bit P and dS on the tensor core, so their error
+scales with their size: max |g - g_ref| <= 2e-2 * (1 + max |g_ref|) for each
+of dQ, dK, dV (the forward's 2e-2 on O, scaled by the gradient's magnitude).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import to_np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_bwd(ea, oracle_mod, b, sq, sk, h, d, dtype, seed):
+    q, k, v = workloads.make_qkv(b, sq, sk, h, d, dtype, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    do = torch.randn((b, sq, h, d), generator=g).to(dtype)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    scale = 1 / math.sqrt(d)
+    o, lse = ea.attn_fwd(qd, kd, vd, scale=scale)
+    dq, dk, dv = ea.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale)
+    status = ea.attn_get_device_status()
+    assert status == ea.ATTN_OK, f"status {status}, site {ea.attn_last_timeout_site():#x}"
+    rq, rk, rv = oracle_mod.attention_backward(q, k, v, do, scale)
+    errs = {}
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        g64 = to_np64(got)
+        assert np.all(np.isfinite(g64)), f"non-finite {name}"
+        err = float(np.abs(g64 - ref).max())
+        bound = 2e-2 * (1.0 + float(np.abs(ref).max()))
+        errs[name] = (err, bound)
+        assert err <= bound, f"{name}: max err {err:.3e} > {bound:.3e} (max |ref| {np.abs(ref).max():.3e})"
+    return errs
+
+
+@pytest.mark.parametrize("b,sq,sk,h,d", [(1, 128, 128, 1, 128), (2, 300, 200, 3, 128),
+                                         (1, 64, 1000, 2, 64), (1, 513, 257, 2, 32),
+                                         (3, 100, 130, 2, 16), (1, 1, 77, 1, 128)])
+def test_bwd_shapes(gpu, oracle_mod, b, sq, sk, h, d):
+    _check_bwd(gpu, oracle_mod, b, sq, sk, h, d, torch.bfloat16, 91)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_bwd_fp16(gpu, oracle_mod, d):
+    _check_bwd(gpu, oracle_mod, 2, 200, 333, 2, d, torch.float16, 93)
+
+
+def test_bwd_many_units_per_cta(gpu, oracle_mod):
+    """More tiles than SMs: every persistent CTA runs several units."""
+    _check_bwd(gpu, oracle_mod, 4, 512, 512, 48, 64, torch.bfloat16, 95)

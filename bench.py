@@ -395,6 +395,19 @@ def measure_extras(ea, dev, flush, stream, peaks):
         out[f"{name}/causal"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
                                  "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
         del q, k, v
+    # backward pass (dQ, dK, dV); FLOP = the five products of the chain
+    # rule, 10*b*h*sq*sk*d (the dQ pass recomputes two of them, not counted)
+    for name in ("mid_fwd", "long_fwd"):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        do = torch.randn((w.b, w.sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        o, lse = ea.attn_fwd(q, k, v, scale=w.scale)
+        fn = lambda: ea.attn_bwd(q, k, v, o, lse, do, scale=w.scale)  # noqa: E731
+        (ms,), _ = time_loop([fn], 10, 3, flush, stream)
+        tf = 10 * w.b * w.h * w.sq * w.sk * w.d / (ms * 1e-3) / 1e12
+        out[f"{name}/backward"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                                   "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, do, o, lse
     # several new query rows share each K/V read (tensor-core decode path)
     for name, sq in (("decode_b8_h48_sk8192", 10), ("decode_b1_h16_sk32768", 10)):
         w = workloads.WORKLOADS[name]

@@ -73,9 +73,12 @@ struct BwdGeom {
     static constexpr int BAR_PF = BAR_SF + 1;
     static constexpr int BAR_AF = BAR_PF + 1;
     static constexpr int BAR_AE = BAR_AF + 1;
-    static constexpr int BAR_DONE = BAR_AE + 1;
+    static constexpr int BAR_LD = BAR_AE + 1;  // [2]: a step's LSE and D staged (dK/dV kernel)
+    static constexpr int BAR_DONE = BAR_LD + 2;
     static constexpr int NUM_BARS = BAR_DONE + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    // per step parity: LSE * log2(e) of the step's 128 query rows, then their D
+    static constexpr int OFF_LD = (OFF_BAR + NUM_BARS * 8 + 15) & ~15;  // read as float4
+    static constexpr int OFF_MISC = OFF_LD + 2 * 2 * BT * 4;
     static constexpr int USED = OFF_MISC + 16;
     static constexpr int MIN_SMEM = 120 * 1024;  // one CTA per SM: it owns all of TMEM
     static constexpr int SMEM_BYTES = (USED > MIN_SMEM ? USED : MIN_SMEM) + 1024;
@@ -310,7 +313,7 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *d
 }
 
 template <int D, int MODE, bool BF16>
-__device__ __forceinline__ void bwd_compute(uint32_t sbase, uint32_t tmem, int q4, int ntiles,
+__device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint32_t tmem, int q4, int ntiles,
                                             int nsteps, int units, const BwdArgs &a,
                                             const WaitGuard &g) {
     using G = BwdGeom<D>;
@@ -334,6 +337,22 @@ __device__ __forceinline__ void bwd_compute(uint32_t sbase, uint32_t tmem, int q
             }
         }
         for (int j = 0; j < nsteps; ++j, ++step) {
+            const float *ldbuf = nullptr;
+            if constexpr (MODE == kBwdDKV) {
+                // Stage the step's LSE (log2 units) and D: thread `row` takes query
+                // row j*128 + row. Double-buffered by step parity; the buffer is
+                // rewritten two steps later, after every warp has passed the
+                // barrier of the step in between.
+                float *buf = reinterpret_cast<float *>(smem + G::OFF_LD) + (step & 1) * 2 * G::BT;
+                const int qr = j * G::BT + row;
+                buf[row] = qr < a.sq ? a.lse[bh * a.sq + qr] * kLog2e : INFINITY;
+                buf[G::BT + row] = qr < a.sq ? a.dvec[bh * a.sq + qr] : 0.f;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(G::BAR_LD + (step & 1)));
+                const bool okl = mbar_wait(bar(G::BAR_LD + (step & 1)), (step >> 1) & 1, g, 15);
+                if (!__all_sync(0xffffffffu, okl)) return;
+                ldbuf = buf;
+            }
             const bool ok = mbar_wait(bar(G::BAR_SF), step & 1, g, 13);
             if (!__all_sync(0xffffffffu, ok)) return;
             tc_fence_after();
@@ -362,37 +381,37 @@ __device__ __forceinline__ void bwd_compute(uint32_t sbase, uint32_t tmem, int q
                 }
             } else {
                 // row = key row; columns = query rows j*128 .. with their own
-                // LSE and D (loads of one address across the warp); query rows
-                // past sq take no part.
-                const int nq = a.sq - j * G::BT;
-                const float *lse_j = a.lse + bh * a.sq + j * G::BT;
-                const float *d_j = a.dvec + bh * a.sq + j * G::BT;
+                // LSE and D, staged for the step in shared memory (query rows
+                // past sq get LSE = +inf, hence P = 0, and D = 0).
+                const float4 *ld4 = reinterpret_cast<const float4 *>(ldbuf);
 #pragma unroll
-                for (int c0 = 0; c0 < G::BT; c0 += 16) {
-                    uint32_t sv[16], pv[16];
-                    tmem_ld16(tmem + lanes + G::T_S + c0, sv);
-                    tmem_ld16(tmem + lanes + G::T_P + c0, pv);
+                for (int c0 = 0; c0 < G::BT; c0 += 32) {
+                    uint32_t sv[32], pv[32];
+                    tmem_ld32(tmem + lanes + G::T_S + c0, sv);
+                    tmem_ld32(tmem + lanes + G::T_P + c0, pv);
                     tmem_wait_ld();
-                    uint32_t pp[8], pd[8];
+                    uint32_t pp[16], pd[16];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float pr[2], dr[2];
+                    for (int q = 0; q < 8; ++q) {  // four columns per shared-memory read
+                        const float4 l4 = ld4[(c0 >> 2) + q];
+                        const float4 d4 = ld4[(G::BT >> 2) + (c0 >> 2) + q];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pr[4], dr[4];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int col = c0 + 2 * i + e;
-                            const bool in = col < nq;
-                            const float l2 = in ? __ldg(lse_j + col) * kLog2e : INFINITY;
-                            const float dd = in ? __ldg(d_j + col) : 0.f;
-                            const float p = in ? fast_exp2(__uint_as_float(sv[2 * i + e]) * c - l2) : 0.f;
-                            pr[e] = p;
-                            dr[e] = p * (__uint_as_float(pv[2 * i + e]) - dd);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * q + e;
+                            pr[e] = fast_exp2(__uint_as_float(sv[i]) * c - lv[e]);
+                            dr[e] = pr[e] * (__uint_as_float(pv[i]) - dv[e]);
                         }
-                        pp[i] = pack2b<BF16>(pr[0], pr[1]);
-                        pd[i] = pack2b<BF16>(dr[0], dr[1]);
+                        pp[2 * q] = pack2b<BF16>(pr[0], pr[1]);
+                        pp[2 * q + 1] = pack2b<BF16>(pr[2], pr[3]);
+                        pd[2 * q] = pack2b<BF16>(dr[0], dr[1]);
+                        pd[2 * q + 1] = pack2b<BF16>(dr[2], dr[3]);
                     }
-                    // P^T and dS^T of columns c0 .. c0+15 into columns c0/2 .. c0/2+7
-                    tmem_st8(tmem + lanes + G::T_S + c0 / 2, pp);
-                    tmem_st8(tmem + lanes + G::T_P + c0 / 2, pd);
+                    // P^T and dS^T of columns c0 .. c0+31 into columns c0/2 .. c0/2+15
+                    tmem_st16(tmem + lanes + G::T_S + c0 / 2, pp);
+                    tmem_st16(tmem + lanes + G::T_P + c0 / 2, pd);
                 }
             }
             tmem_wait_st();
@@ -449,7 +468,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i)
-            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_AE) ? 4u : 1u);  // one per compute warp
+            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_AE || i == G::BAR_LD || i == G::BAR_LD + 1)
+                                  ? 4u    // one per compute warp
+                                  : 1u);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -474,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) bwd_mma<D, MODE, BF16>(sbase, tmem, nsteps, units, g);
     } else if (warp >= 4 && warp < 8) {
-        bwd_compute<D, MODE, BF16>(sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
+        bwd_compute<D, MODE, BF16>(smem, sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
     }
 
     tc_fence_before();

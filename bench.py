@@ -518,6 +518,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-problem extra timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--backward", action="store_true",
+                    help="with --profile-only on a forward workload: run its backward pass instead")
     ap.add_argument("--profile-only", choices=sorted(workloads.WORKLOADS), default=None,
                     help="profiling aid: only run warmup + steps calls of one workload's kernels "
                          "(no timing, no JSON line), e.g. under ncu")
@@ -550,6 +552,12 @@ def run_profile_only(args):
     v = torch.randn((w.b, w.sk, w.h, w.d), generator=gen, device=dev).to(w.dtype)
     fn = (lambda: ea.attn_fwd(q, k, v)) if w.kind == "fwd" else (
         lambda: ea.attn_decode_splitkv(q, k, v, num_splits=0))
+    if args.backward:
+        if w.kind != "fwd":
+            raise SystemExit("--backward needs a forward workload")
+        do = torch.randn((w.b, w.sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        o, lse = ea.attn_fwd(q, k, v)
+        fn = lambda: ea.attn_bwd(q, k, v, o, lse, do)  # noqa: E731
     for _ in range(args.warmup + args.steps):
         fn()
     if ea.attn_get_device_status() != ea.ATTN_OK:

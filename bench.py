@@ -407,6 +407,14 @@ def measure_extras(ea, dev, flush, stream, peaks):
         tf = 10 * w.b * w.h * w.sq * w.sk * w.d / (ms * 1e-3) / 1e12
         out[f"{name}/backward"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
                                    "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
+        # causal backward: the five products over the unmasked scores only
+        o, lse = ea.attn_fwd(q, k, v, scale=w.scale, causal=True)
+        fn = lambda: ea.attn_bwd(q, k, v, o, lse, do, scale=w.scale,  # noqa: E731
+                                 causal=True)
+        (ms,), _ = time_loop([fn], 10, 3, flush, stream)
+        tf = 10 * w.b * w.h * w.d * (w.sq * (w.sq + 1) // 2) / (ms * 1e-3) / 1e12
+        out[f"{name}/backward_causal"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                                          "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
         del q, k, v, do, o, lse
     # several new query rows share each K/V read (tensor-core decode path)
     for name, sq in (("decode_b8_h48_sk8192", 10), ("decode_b1_h16_sk32768", 10)):

@@ -70,8 +70,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_paged.restype = i32
         lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                           i32, f32, i32, i32, vp]
-        lib.attn_bwd.restype = i32
-        lib.attn_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, i32, vp]
+        for fn in (lib.attn_bwd, lib.attn_bwd_causal):
+            fn.restype = i32
+            fn.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, i32, vp]
         lib.attn_decode_num_splits.restype = i32
         lib.attn_decode_num_splits.argtypes = [i32] * 5
         lib.attn_decode_num_splits_for_sms.restype = i32
@@ -224,11 +225,12 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float 
 
 
 def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None, dv=None,
-             stream=None):
-    """Backward pass of attn_fwd (non-causal): returns (dq, dk, dv).
+             stream=None, causal: bool = False):
+    """Backward pass of attn_fwd: returns (dq, dk, dv).
 
     q, o, dout: [b, sq, h, d]; k, v: [b, sk, h, d] (fp16 or bf16, contiguous
-    CUDA tensors); lse: fp32 [b, h, sq] from attn_fwd."""
+    CUDA tensors); lse: fp32 [b, h, sq] from attn_fwd with the same
+    ``causal`` (the bottom-right-aligned mask, attn_bwd_causal)."""
     b, sq, sk, h, d, dt = _check(q, k, v)
     for name, t in (("o", o), ("dout", dout)):
         if not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != q.dtype \
@@ -246,11 +248,12 @@ def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None
             raise ValueError(f"{name} must be a contiguous tensor like {name[1]}")
     lib = load_library()
     with torch.cuda.device(q.device):
-        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                          b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+        fn = lib.attn_bwd_causal if causal else lib.attn_bwd
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd")
+        raise AttnError(rc, "attn_bwd_causal" if causal else "attn_bwd")
     return dq, dk, dv
 
 

@@ -256,10 +256,10 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
                    stream);
 }
 
-attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                       const float *lse, const void *dout, void *dq, void *dk, void *dv, int b,
-                       int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
-                       cudaStream_t stream) {
+static attn_status_t run_bwd(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                             bool causal, cudaStream_t stream) {
     attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
     if (!dout || !dq || !dk || !dv || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) ||
@@ -293,6 +293,7 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
     a.status = ds->status;
     a.flags = debug_flags();
     a.num_sms = ds->num_sms;
+    a.causal = causal ? 1 : 0;
     // D = rowsum(dO * O), fp32 [b, h, sq], from the stream-ordered pool
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, static_cast<size_t>(b) * h * sq * sizeof(float), stream) !=
@@ -304,6 +305,22 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
     const cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv, int b,
+                       int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+    return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, b, sq, sk, h, d, scale, dtype, false,
+                   stream);
+}
+
+attn_status_t attn_bwd_causal(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                              int b, int sq, int sk, int h, int d, float scale,
+                              attn_dtype_t dtype, cudaStream_t stream) {
+    return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, b, sq, sk, h, d, scale, dtype, true,
+                   stream);
 }
 
 int attn_decode_num_splits_for_sms(int b, int sq, int sk, int h, int d, int num_sms) {

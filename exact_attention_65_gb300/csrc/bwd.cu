@@ -145,20 +145,59 @@ struct BUnit {
     int tile, head, batch;
 };
 
-__device__ __forceinline__ BUnit bunit_of(int u, int ntiles, int h) {
+// Without a mask the tiles of one (batch, head) are neighbours, so CTAs
+// running at the same time share its streamed tiles in L2. Under the causal
+// mask units differ in length (a query tile's grows with its index, a key
+// tile's shrinks), and a grid that is a multiple of the tile count would keep
+// each CTA on one tile index; there units run longest first across all
+// (batch, head) pairs, so the round-robin over CTAs deals each a mix.
+template <int MODE, bool CAUSAL>
+__device__ __forceinline__ BUnit bunit_of(int u, int ntiles, const BwdArgs &a) {
     BUnit x;
-    x.tile = u % ntiles;
-    const int r = u / ntiles;
-    x.head = r % h;
-    x.batch = r / h;
+    int r;
+    if constexpr (CAUSAL) {
+        const int bh = a.b * a.h;
+        const int rank = u / bh;
+        r = u - rank * bh;
+        x.tile = MODE == kBwdDQ ? ntiles - 1 - rank : rank;
+    } else {
+        x.tile = u % ntiles;
+        r = u / ntiles;
+    }
+    x.head = r % a.h;
+    x.batch = r / a.h;
     return x;
 }
 
-template <int D, int MODE>
+// The streamed tiles a unit visits: first .. first + count - 1 of nsteps_all.
+// With the causal mask (query row i sees key k only if k <= i + sk - sq) a
+// query tile stops at its last row's last visible key tile, and a key tile
+// starts at the first query tile that can see any of its keys; a unit with
+// nothing left (count 0) writes zeros.
+template <int MODE, bool CAUSAL>
+__device__ __forceinline__ void unit_steps(const BUnit &x, int nsteps_all, const BwdArgs &a,
+                                           int &first, int &count) {
+    first = 0;
+    count = nsteps_all;
+    if constexpr (CAUSAL) {
+        const int off = a.sk - a.sq;
+        if constexpr (MODE == kBwdDQ) {
+            const int last = min(x.tile * 128 + 127, a.sq - 1);
+            const int kmax = last + off;
+            count = kmax < 0 ? 0 : min(nsteps_all, kmax / 128 + 1);
+        } else {
+            const int q0 = x.tile * 128 - off;  // first query row seeing the tile's first key
+            first = q0 <= 0 ? 0 : min(q0 / 128, nsteps_all);
+            count = nsteps_all - first;
+        }
+    }
+}
+
+template <int D, int MODE, bool CAUSAL>
 __device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                              const CUtensorMap *tv, const CUtensorMap *tdo,
                                              uint32_t sbase, int ntiles, int nsteps, int units,
-                                             int h, const WaitGuard &g) {
+                                             const BwdArgs &a, const WaitGuard &g) {
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     // the unit's fixed pair and the streamed pair of each step
@@ -170,7 +209,9 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtens
     int it_u = 0, n_issued = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
-        const BUnit x = bunit_of(u, ntiles, h);
+        const BUnit x = bunit_of<MODE, CAUSAL>(u, ntiles, a);
+        int first, count;
+        unit_steps<MODE, CAUSAL>(x, nsteps, a, first, count);
         if (!mbar_wait(bar(G::BAR_FE), (it_u & 1) ^ 1, g, 1)) break;
         mbar_arrive_expect_tx(bar(G::BAR_FF), 2 * G::TILE_BYTES);
         for (int p = 0; p < G::PANELS; ++p) {
@@ -179,7 +220,7 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtens
             tma_load_4d(sbase + G::OFF_FIX + G::TILE_BYTES + p * G::PANEL_BYTES, fb, bar(G::BAR_FF),
                         p * G::PANEL_ELEMS, x.head, x.tile * G::BT, x.batch);
         }
-        for (int i = 0; i < 2 * nsteps; ++i) {  // step j: item 2j from sa, 2j + 1 from sb
+        for (int i = 0; i < 2 * count; ++i) {  // step j: item 2j from sa, 2j + 1 from sb
             const int s = n_issued % G::SLOTS;
             if (!mbar_wait(bar(G::BAR_RE + s), ((n_issued / G::SLOTS) & 1) ^ 1, g, 2)) {
                 ok = false;
@@ -189,8 +230,8 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtens
             const CUtensorMap *map = (i & 1) ? sb : sa;
             for (int p = 0; p < G::PANELS; ++p)
                 tma_load_4d_hint(sbase + G::OFF_RING + s * G::TILE_BYTES + p * G::PANEL_BYTES, map,
-                                 bar(G::BAR_RF + s), p * G::PANEL_ELEMS, x.head, (i >> 1) * G::BT,
-                                 x.batch, keep);
+                                 bar(G::BAR_RF + s), p * G::PANEL_ELEMS, x.head,
+                                 (first + (i >> 1)) * G::BT, x.batch, keep);
             ++n_issued;
         }
     }
@@ -203,9 +244,9 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap *tq, const CUtens
         mbar_wait(bar(G::BAR_RF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
 }
 
-template <int D, int MODE, bool BF16>
-__device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int nsteps, int units,
-                                        const WaitGuard &g) {
+template <int D, int MODE, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntiles, int nsteps,
+                                        int units, const BwdArgs &a, const WaitGuard &g) {
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     constexpr uint32_t idesc_sq = mma_idesc_f16(G::BT, G::BT, BF16, false, false);  // 128x128 tiles
@@ -238,7 +279,14 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int nstep
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
         if (!mbar_wait(bar(G::BAR_FF), it_u & 1, g, 4)) break;
-        for (int j = 0; j < nsteps; ++j) {
+        int first, count;
+        unit_steps<MODE, CAUSAL>(bunit_of<MODE, CAUSAL>(u, ntiles, a), nsteps, a, first, count);
+        if (count == 0) {  // nothing to accumulate: free the fixed tiles, hand over
+            mma_commit(bar(G::BAR_FE));
+            mma_commit(bar(G::BAR_AF));
+            continue;
+        }
+        for (int j = 0; j < count; ++j) {
             const int na = 2 * (base + j), nb = na + 1;
             const int sa = na % G::SLOTS, sb = nb % G::SLOTS;
             if (!mbar_wait(bar(G::BAR_RF + sa), (na / G::SLOTS) & 1, g, 5) ||
@@ -277,12 +325,12 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int nstep
             }
             mma_commit(bar(G::BAR_RE + sa));
             mma_commit(bar(G::BAR_RE + sb));
-            if (j == nsteps - 1) {
+            if (j == count - 1) {
                 mma_commit(bar(G::BAR_FE));
                 mma_commit(bar(G::BAR_AF));
             }
         }
-        base += nsteps;
+        base += count;
     }
     mma_commit(bar(G::BAR_DONE));
     WaitGuard drain = g;
@@ -294,7 +342,8 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int nstep
 // Store `cols` columns (multiple of 16) of one fp32 TMEM row, scaled, as
 // 16-bit values at dst.
 template <int COLS, bool BF16>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *dst, bool out) {
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *dst, bool out,
+                                          bool zero) {
 #pragma unroll
     for (int c0 = 0; c0 < COLS; c0 += 16) {
         uint32_t v[16];
@@ -304,7 +353,9 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *d
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                pk[i] = pack2b<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+                pk[i] = zero ? 0u
+                             : pack2b<BF16>(__uint_as_float(v[2 * i]) * mul,
+                                            __uint_as_float(v[2 * i + 1]) * mul);
             uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
             d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -312,7 +363,7 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *d
     }
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint32_t tmem, int q4, int ntiles,
                                             int nsteps, int units, const BwdArgs &a,
                                             const WaitGuard &g) {
@@ -325,7 +376,9 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
     constexpr float kLog2e = 1.4426950408889634f;
     int it_u = 0, step = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++it_u) {
-        const BUnit x = bunit_of(u, ntiles, a.h);
+        const BUnit x = bunit_of<MODE, CAUSAL>(u, ntiles, a);
+        int first, count;
+        unit_steps<MODE, CAUSAL>(x, nsteps, a, first, count);
         const int grow = x.tile * G::BT + row;
         const int64_t bh = static_cast<int64_t>(x.batch) * a.h + x.head;
         // dQ kernel: this row's LSE (log2 units) and D; rows past sq take no part
@@ -336,7 +389,8 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                 drow = a.dvec[bh * a.sq + grow];
             }
         }
-        for (int j = 0; j < nsteps; ++j, ++step) {
+        for (int j = 0; j < count; ++j, ++step) {
+            const int tj = first + j;  // the streamed tile of this step
             const float *ldbuf = nullptr;
             if constexpr (MODE == kBwdDKV) {
                 // Stage the step's LSE (log2 units) and D: thread `row` takes query
@@ -344,7 +398,7 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                 // rewritten two steps later, after every warp has passed the
                 // barrier of the step in between.
                 float *buf = reinterpret_cast<float *>(smem + G::OFF_LD) + (step & 1) * 2 * G::BT;
-                const int qr = j * G::BT + row;
+                const int qr = tj * G::BT + row;
                 buf[row] = qr < a.sq ? a.lse[bh * a.sq + qr] * kLog2e : INFINITY;
                 buf[G::BT + row] = qr < a.sq ? a.dvec[bh * a.sq + qr] : 0.f;
                 __syncwarp();
@@ -359,7 +413,8 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
             if constexpr (MODE == kBwdDQ) {
                 // row = query row; columns = keys j*128 .. : P = 2^(s c - lse2),
                 // dS = P (dP - D); keys past sk (TMA zero fill) take no part.
-                const int kv = a.sk - j * G::BT;
+                // (causal: the row's own last visible key)
+                const int kv = (CAUSAL ? min(a.sk, grow + a.sk - a.sq + 1) : a.sk) - tj * G::BT;
 #pragma unroll
                 for (int c0 = 0; c0 < G::BT; c0 += 32) {
                     uint32_t sv[32], pv[32];
@@ -384,6 +439,8 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                 // LSE and D, staged for the step in shared memory (query rows
                 // past sq get LSE = +inf, hence P = 0, and D = 0).
                 const float4 *ld4 = reinterpret_cast<const float4 *>(ldbuf);
+                // causal: this key row is seen by query columns >= cmin
+                const int cmin = CAUSAL ? grow - (a.sk - a.sq) - tj * G::BT : -1;
 #pragma unroll
                 for (int c0 = 0; c0 < G::BT; c0 += 32) {
                     uint32_t sv[32], pv[32];
@@ -402,6 +459,7 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                         for (int e = 0; e < 4; ++e) {
                             const int i = 4 * q + e;
                             pr[e] = fast_exp2(__uint_as_float(sv[i]) * c - lv[e]);
+                            if constexpr (CAUSAL) pr[e] = (c0 + i >= cmin) ? pr[e] : 0.f;
                             dr[e] = pr[e] * (__uint_as_float(pv[i]) - dv[e]);
                         }
                         pp[2 * q] = pack2b<BF16>(pr[0], pr[1]);
@@ -429,14 +487,15 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
             const bool out = grow < a.sq;
             uint16_t *dst = reinterpret_cast<uint16_t *>(a.dq) +
                             ((static_cast<int64_t>(x.batch) * a.sq + (out ? grow : 0)) * a.h + x.head) * D;
-            store_row<D, BF16>(tmem + lanes + G::T_A0, scale, dst, out);
+            store_row<D, BF16>(tmem + lanes + G::T_A0, scale, dst, out, count == 0);
         } else {
             const bool out = grow < a.sk;
             const int64_t off =
                 ((static_cast<int64_t>(x.batch) * a.sk + (out ? grow : 0)) * a.h + x.head) * D;
-            store_row<D, BF16>(tmem + lanes + G::T_A0, 1.0f, reinterpret_cast<uint16_t *>(a.dv) + off, out);
+            store_row<D, BF16>(tmem + lanes + G::T_A0, 1.0f, reinterpret_cast<uint16_t *>(a.dv) + off, out,
+                               count == 0);
             store_row<D, BF16>(tmem + lanes + G::T_A1, scale, reinterpret_cast<uint16_t *>(a.dk) + off,
-                               out);
+                               out, count == 0);
         }
         tc_fence_before();
         __syncwarp();
@@ -444,7 +503,7 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
     }
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -490,12 +549,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tdo);
-            bwd_producer<D, MODE>(&tq, &tk, &tv, &tdo, sbase, ntiles, nsteps, units, a.h, g);
+            bwd_producer<D, MODE, CAUSAL>(&tq, &tk, &tv, &tdo, sbase, ntiles, nsteps, units, a, g);
         }
     } else if (warp == 1) {
-        if (lane == 0) bwd_mma<D, MODE, BF16>(sbase, tmem, nsteps, units, g);
+        if (lane == 0) bwd_mma<D, MODE, BF16, CAUSAL>(sbase, tmem, ntiles, nsteps, units, a, g);
     } else if (warp >= 4 && warp < 8) {
-        bwd_compute<D, MODE, BF16>(smem, sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
+        bwd_compute<D, MODE, BF16, CAUSAL>(smem, sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
     }
 
     tc_fence_before();
@@ -504,7 +563,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
     using G = BwdGeom<D>;
@@ -513,7 +572,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(bwd_kernel<D, MODE, BF16>,
+        e = cudaFuncSetAttribute(bwd_kernel<D, MODE, BF16, CAUSAL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -521,7 +580,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     const int64_t ntiles = MODE == kBwdDQ ? (a.sq + G::BT - 1) / G::BT : (a.sk + G::BT - 1) / G::BT;
     const int64_t units = ntiles * a.h * a.b;
     const int64_t ctas = units < a.num_sms ? units : a.num_sms;
-    bwd_kernel<D, MODE, BF16>
+    bwd_kernel<D, MODE, BF16, CAUSAL>
         <<<static_cast<unsigned>(ctas), kBwdThreads, G::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }
@@ -538,9 +597,14 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
         a.sq, a.h);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_bwd_t<D, kBwdDKV, BF16>(tq, tk, tv, tdo, a, stream);
+    if (a.causal) {
+        e = launch_bwd_t<D, kBwdDKV, BF16, true>(tq, tk, tv, tdo, a, stream);
+        if (e != cudaSuccess) return e;
+        return launch_bwd_t<D, kBwdDQ, BF16, true>(tq, tk, tv, tdo, a, stream);
+    }
+    e = launch_bwd_t<D, kBwdDKV, BF16, false>(tq, tk, tv, tdo, a, stream);
     if (e != cudaSuccess) return e;
-    return launch_bwd_t<D, kBwdDQ, BF16>(tq, tk, tv, tdo, a, stream);
+    return launch_bwd_t<D, kBwdDQ, BF16, false>(tq, tk, tv, tdo, a, stream);
 }
 
 }  // namespace

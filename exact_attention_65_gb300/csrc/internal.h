@@ -59,6 +59,7 @@ struct BwdArgs {
     uint32_t *status;
     uint32_t flags;
     int num_sms;
+    int causal;  // the forward's bottom-right-aligned causal mask
 };
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,

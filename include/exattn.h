@@ -93,6 +93,19 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
                        cudaStream_t stream);
 
 /*
+ * Backward pass of attn_fwd_causal: the same chain rule with P = 0 wherever
+ * the forward's bottom-right-aligned mask hides a key (key j of row i is
+ * hidden when j > i + sk - sq). lse must be the one attn_fwd_causal wrote
+ * (-inf for rows that see no key; those rows get dq = 0, and keys that no
+ * row sees get dk = dv = 0). Tiles that the mask hides wholly are skipped.
+ * Arguments, layouts, workspace and errors are those of attn_bwd.
+ */
+attn_status_t attn_bwd_causal(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                              int b, int sq, int sk, int h, int d, float scale,
+                              attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * Split-KV decode, bf16 q/k/v/o ("where is flash decoding second stage
  * (reduce) code?" issue). seqlen_k is cut into num_splits ranges of whole
  * key blocks; split i writes its own O_i and LSE_i (fp32, library

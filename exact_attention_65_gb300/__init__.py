@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_splitkv_ex.restype = i32
         lib.attn_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp]
+        lib.attn_fwd_host.restype = i32
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
         lib.attn_fwd_causal.restype = i32
         lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
         lib.attn_decode_splitkv_causal.restype = i32
@@ -160,6 +162,52 @@ def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=Non
                 b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_causal" if causal else "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_host(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False,
+                  device=None, stream=None, sync: bool = True):
+    """attn_fwd on host (CPU) tensors through the library's copy / compute /
+    copy-back pipeline (attn_fwd_host in the C ABI).
+
+    q: [b, sq, h, d], k/v: [b, sk, h, d], fp16 or bf16, contiguous CPU
+    tensors, best in pinned memory (pageable ones work, without overlap).
+    out and lse (CPU) are allocated pinned when not given. Runs on
+    ``device`` (default: the current CUDA device) and ``stream`` (its
+    current stream). With ``sync`` False the call returns once the work is
+    queued: out and lse are valid, and the inputs may be reused, only after
+    the stream is synchronised."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{name} must be a CPU tensor (attn_fwd takes CUDA tensors)")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [b, s, h, d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    b, sq, h, d = q.shape
+    if k.shape != v.shape or k.shape[0] != b or k.shape[2] != h or k.shape[3] != d:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    dt = _dtype_code(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device.type != "cpu":
+        raise ValueError("out must be a contiguous CPU tensor like q")
+    if lse is None:
+        lse = torch.empty((b, h, sq), dtype=torch.float32, pin_memory=True)
+    elif (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
+          or lse.device.type != "cpu"):
+        raise ValueError("lse must be a contiguous float32 CPU tensor [b, h, sq]")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    lib = load_library()
+    with torch.cuda.device(device):
+        st = _stream(device, stream)
+        rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), b, sq, k.shape[1], h, d, scale, dt, 1 if causal else 0, st)
+        if rc != ATTN_OK:
+            raise AttnError(rc, "attn_fwd_host")
+        if sync:
+            (torch.cuda.current_stream(device) if stream is None else stream).synchronize()
     return out, lse
 
 
@@ -287,7 +335,8 @@ def attn_debug_set_flags(flags: int) -> None:
 
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_num_splits",
+    "AttnError", "attn_fwd", "attn_fwd_host", "attn_bwd", "attn_decode_splitkv",
+    "attn_decode_paged", "attn_decode_num_splits",
     "attn_decode_num_splits_for_sms", "attn_get_device_status", "attn_last_timeout_site",
     "attn_release_workspace", "attn_debug_set_flags", "attn_status_string", "load_library",
 ]

@@ -79,6 +79,8 @@ struct DeviceState {
     bool ready = false;
     uint32_t *status = nullptr;  // device word written by kernels that give up a wait
     int num_sms = 0;
+    // copy streams of the host-buffer forward, made on first use
+    cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -113,6 +115,21 @@ attn_status_t device_state(DeviceState **out) {
         st.ready = true;
     }
     *out = &st;
+    return ATTN_OK;
+}
+
+// The two copy streams of the host-buffer forward (non-blocking, kept for the
+// life of the process).
+attn_status_t copy_streams(DeviceState *ds) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!ds->s_h2d && cudaStreamCreateWithFlags(&ds->s_h2d, cudaStreamNonBlocking) != cudaSuccess) {
+        ds->s_h2d = nullptr;
+        return ATTN_ERR_CUDA;
+    }
+    if (!ds->s_d2h && cudaStreamCreateWithFlags(&ds->s_d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        ds->s_d2h = nullptr;
+        return ATTN_ERR_CUDA;
+    }
     return ATTN_OK;
 }
 
@@ -254,6 +271,133 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     return run_fwd(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype == ATTN_BF16, 1, true, ds,
                    stream);
+}
+
+namespace {
+
+constexpr int kHostChunks = 8;  // most batch chunks of the host-buffer forward
+constexpr int kHostRowChunks = 4;
+
+struct HostChunk {
+    int b0, nb;  // batches
+    int r0, nr;  // query rows (all of them unless one batch is cut by rows)
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                            int causal, cudaStream_t stream) {
+    attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
+    if (st != ATTN_OK) return st;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != ATTN_OK) return st;
+    if ((st = copy_streams(ds)) != ATTN_OK) return st;
+    const bool bf16 = dtype == ATTN_BF16;
+    const size_t row = static_cast<size_t>(h) * d * 2;  // bytes of one sequence position
+    const size_t qbat = row * sq, kbat = row * sk, lbat = static_cast<size_t>(h) * sq * sizeof(float);
+
+    // The plan: whole batches per chunk; a single non-causal batch is cut
+    // into ranges of query rows (multiples of the kernel's 256-row block, so
+    // every row sees the same tiles as in one call) after K and V are in.
+    HostChunk plan[kHostChunks];
+    int n = 0;
+    bool by_rows = false;
+    if (b >= 2) {
+        const int nc = b < kHostChunks ? b : kHostChunks;
+        for (int i = 0; i < nc; ++i) {
+            const int b0 = static_cast<int>(static_cast<int64_t>(b) * i / nc);
+            const int b1 = static_cast<int>(static_cast<int64_t>(b) * (i + 1) / nc);
+            plan[n++] = HostChunk{b0, b1 - b0, 0, sq};
+        }
+    } else if (!causal && sq >= 2 * FWD_BM * FWD_QTILES) {
+        const int blk = FWD_BM * FWD_QTILES;
+        const int per = static_cast<int>(cdiv(cdiv(sq, kHostRowChunks), blk) * blk);
+        for (int r0 = 0; r0 < sq; r0 += per) plan[n++] = HostChunk{0, 1, r0, sq - r0 < per ? sq - r0 : per};
+        by_rows = n > 1;
+    } else {
+        plan[n++] = HostChunk{0, b, 0, sq};
+    }
+
+    // Device workspace Q, K, V, O, LSE (+ per-row-chunk LSE [h, rows]), one
+    // stream-ordered allocation on `stream`.
+    const size_t oq = 0, ok_ = round_up(oq + qbat * b, 256), ov = round_up(ok_ + kbat * b, 256),
+                 oo = round_up(ov + kbat * b, 256), ol = round_up(oo + qbat * b, 256),
+                 ot = round_up(ol + lbat * b, 256), total = ot + (by_rows ? lbat : 0);
+    char *ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), total, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_MEMORY;
+    }
+    cudaEvent_t ev[2 * kHostChunks + 2] = {};
+    const int nev = 2 * n + 2;
+    bool good = true;
+    for (int i = 0; i < nev && good; ++i)
+        good = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    cudaEvent_t ev_start = ev[2 * n], ev_end = ev[2 * n + 1];
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
+               *hv = static_cast<const char *>(v);
+    char *ho = static_cast<char *>(o);
+    auto h2d = [&](size_t off_dev, const char *src, size_t bytes) {
+        if (good) good = cudaMemcpyAsync(ws + off_dev, src, bytes, cudaMemcpyHostToDevice, ds->s_h2d) == cudaSuccess;
+    };
+    // the copy streams start after the allocation and whatever precedes the call
+    if (good) good = cudaEventRecord(ev_start, stream) == cudaSuccess;
+    if (good) good = cudaStreamWaitEvent(ds->s_h2d, ev_start, 0) == cudaSuccess;
+    if (good) good = cudaStreamWaitEvent(ds->s_d2h, ev_start, 0) == cudaSuccess;
+    for (int c = 0; c < n && good; ++c) {
+        const HostChunk &x = plan[c];
+        // in: K and V of the chunk's batches (once, when cut by rows), then its Q rows
+        if (!by_rows || c == 0) {
+            h2d(ok_ + kbat * x.b0, hk + kbat * x.b0, kbat * x.nb);
+            h2d(ov + kbat * x.b0, hv + kbat * x.b0, kbat * x.nb);
+        }
+        const size_t qoff = qbat * x.b0 + row * x.r0, qbytes = by_rows ? row * x.nr : qbat * x.nb;
+        h2d(oq + qoff, hq + qoff, qbytes);
+        if (good) good = cudaEventRecord(ev[2 * c], ds->s_h2d) == cudaSuccess;
+        // compute on the caller's stream
+        if (good) good = cudaStreamWaitEvent(stream, ev[2 * c], 0) == cudaSuccess;
+        float *lse_dev = by_rows ? reinterpret_cast<float *>(ws + ot) + static_cast<size_t>(h) * x.r0
+                                 : reinterpret_cast<float *>(ws + ol) + static_cast<size_t>(h) * sq * x.b0;
+        if (good)
+            good = run_fwd(ws + oq + qoff, ws + ok_ + kbat * x.b0, ws + ov + kbat * x.b0, ws + oo + qoff,
+                           lse_dev, x.nb, x.nr, sk, h, d, scale, bf16, 1, causal != 0, ds,
+                           stream) == ATTN_OK;
+        if (good) good = cudaEventRecord(ev[2 * c + 1], stream) == cudaSuccess;
+        // out: O rows and LSE on the second copy stream
+        if (good) good = cudaStreamWaitEvent(ds->s_d2h, ev[2 * c + 1], 0) == cudaSuccess;
+        if (good)
+            good = cudaMemcpyAsync(ho + qoff, ws + oo + qoff, qbytes, cudaMemcpyDeviceToHost,
+                                   ds->s_d2h) == cudaSuccess;
+        if (good) {
+            if (by_rows)  // LSE [h, rows] into the rows' columns of [h, sq]
+                good = cudaMemcpy2DAsync(lse + x.r0, static_cast<size_t>(sq) * sizeof(float), lse_dev,
+                                         static_cast<size_t>(x.nr) * sizeof(float),
+                                         static_cast<size_t>(x.nr) * sizeof(float), h,
+                                         cudaMemcpyDeviceToHost, ds->s_d2h) == cudaSuccess;
+            else
+                good = cudaMemcpyAsync(lse + static_cast<size_t>(h) * sq * x.b0, lse_dev, lbat * x.nb,
+                                       cudaMemcpyDeviceToHost, ds->s_d2h) == cudaSuccess;
+        }
+    }
+    // Join: the caller's stream waits for both copy streams (also after an
+    // error, so that the workspace is freed only when nothing uses it).
+    bool joined = ev_end != nullptr;
+    if (joined) joined = cudaEventRecord(ev_end, ds->s_h2d) == cudaSuccess;
+    if (joined) joined = cudaStreamWaitEvent(stream, ev_end, 0) == cudaSuccess;
+    if (joined) joined = cudaEventRecord(ev_end, ds->s_d2h) == cudaSuccess;
+    if (joined) joined = cudaStreamWaitEvent(stream, ev_end, 0) == cudaSuccess;
+    if (!joined) {
+        // without the join the copy streams may still use the workspace
+        cudaStreamSynchronize(ds->s_h2d);
+        cudaStreamSynchronize(ds->s_d2h);
+    }
+    const bool freed = cudaFreeAsync(ws, stream) == cudaSuccess;
+    for (int i = 0; i < nev; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    return (good && joined && freed) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 static attn_status_t run_bwd(const void *q, const void *k, const void *v, const void *o,

@@ -74,6 +74,30 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
                               attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_fwd (causal != 0: attn_fwd_causal) on HOST buffers: q, k, v, o, lse
+ * as in attn_fwd but in host memory, 16-byte aligned; pinned memory
+ * (cudaHostAlloc, cudaHostRegister) lets the copies overlap, pageable
+ * memory works but its copies serialise with the host. The call runs a
+ * copy / compute / copy-back pipeline: the problem is cut into chunks of
+ * whole batches (at most 8), or, for one non-causal batch of at least 512
+ * query rows, into at most 4 ranges of query rows that are multiples of 256
+ * (K and V go first); the chunk's inputs go up on a library copy stream,
+ * its forward runs on `stream`, and its O and LSE come back on a second
+ * copy stream while the next chunk goes up. Results are bit-identical to
+ * attn_fwd on device copies of the same inputs. Device workspace for all
+ * five tensors is taken stream-ordered from the device's default memory
+ * pool on `stream` and returned. The call is stream-ordered on `stream`:
+ * it starts after the work already queued there, and work queued there
+ * afterwards starts once every copy-back is done, so o and lse may be read
+ * after `stream` is synchronised (the host buffers must stay valid until
+ * then). Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be
+ * had.
+ */
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
+                            int causal, cudaStream_t stream);
+
+/*
  * Backward pass of attn_fwd (non-causal): dq, dk, dv from q, k, v, the
  * forward's o and lse, and the upstream gradient dout. The flash-attn timing
  * issue times a backward pass; none of the pages writes one out, so it is

@@ -74,6 +74,23 @@ def test_fwd_validation(exattn_lib, kw, expect):
 
 
 @pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), ea.ATTN_ERR_INVALID_ARG),
+    (dict(o=ALIGNED + 8), ea.ATTN_ERR_INVALID_ARG),
+    (dict(sq=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), ea.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+])
+def test_fwd_host_validation(exattn_lib, kw, expect):
+    """The host-buffer forward checks its arguments before any CUDA call."""
+    args = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, o=ALIGNED, lse=ALIGNED, b=1, sq=8, sk=8, h=1, d=64,
+                scale=0.125)
+    args.update(kw)
+    a = args
+    assert exattn_lib.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["b"], a["sq"], a["sk"],
+                                    a["h"], a["d"], a["scale"], ea.ATTN_BF16, 0, None) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
     (dict(v=None), ea.ATTN_ERR_INVALID_ARG),
     (dict(o=ALIGNED + 4), ea.ATTN_ERR_INVALID_ARG),
     (dict(sk=0), ea.ATTN_ERR_INVALID_ARG),

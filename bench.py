@@ -24,6 +24,7 @@ bounded sample of the same forward problem, on rank 0's host cores.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -357,6 +358,32 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def host_call_us(ea, q, k, v, w, stream, calls=200):
+    """Host time to issue one forward (small problems are dominated by it):
+    the Python binding and the bare C-ABI call, each averaged over `calls`
+    calls issued while the GPU is held busy, so the host never waits."""
+    lib = ea.load_library()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.b, w.h, w.sq), dtype=torch.float32, device=q.device)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    dt = ea.ATTN_BF16 if w.dtype == torch.bfloat16 else ea.ATTN_FP16
+    res = {}
+    for label, fn in (
+            ("python", lambda: ea.attn_fwd(q, k, v, scale=w.scale, out=o, lse=lse)),
+            ("c_abi", lambda: lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           lse.data_ptr(), w.b, w.sq, w.sk, w.h, w.d, w.scale, dt,
+                                           st))):
+        fn()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e8))  # about 0.1 s of GPU time at ~2 GHz
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        res[label] = round((time.perf_counter() - t0) / calls * 1e6, 2)
+        torch.cuda.synchronize()
+    return res
+
+
 def measure_extras(ea, dev, flush, stream, peaks):
     """Per-problem kernel times for the other workloads (20 timed calls each)."""
     out = {}
@@ -379,6 +406,8 @@ def measure_extras(ea, dev, flush, stream, peaks):
         out[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
                      "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
                      "GB/s": round(w.io_bytes / (ms * 1e-3) / 1e9, 1)}
+        if name != "long_fwd":
+            out[name]["host_call_us"] = host_call_us(ea, q, k, v, w, stream)
         del q, k, v
     # causal forward (bottom-right aligned; sq == sk here): FLOP counts only
     # the unmasked scores, 4*b*h*d * sum over rows of the keys a row sees

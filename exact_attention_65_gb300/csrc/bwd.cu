@@ -48,6 +48,7 @@ constexpr int kBwdThreads = 256;
 template <int D>
 struct BwdGeom {
     static constexpr int BT = 128;  // rows of every tile
+    static constexpr int HN = 64;   // a step's score tile is made and used in two halves of HN columns
     static constexpr int ROW_BYTES = fwd_row_bytes(D);
     static constexpr int PANELS = (D * 2) / ROW_BYTES;
     static constexpr int PANEL_ELEMS = ROW_BYTES / 2;
@@ -64,14 +65,14 @@ struct BwdGeom {
     static constexpr int OFF_RING = 2 * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_RING + SLOTS * TILE_BYTES;
     // barriers: fix_full | fix_empty | ring_full[SLOTS] | ring_empty[SLOTS] |
-    //           s_full | p_full | acc_full | acc_empty | done
+    //           s_full[2] | p_full[2] | acc_full | acc_empty | ld[2] | done
     static constexpr int BAR_FF = 0;
     static constexpr int BAR_FE = 1;
     static constexpr int BAR_RF = 2;
     static constexpr int BAR_RE = BAR_RF + SLOTS;
-    static constexpr int BAR_SF = BAR_RE + SLOTS;
-    static constexpr int BAR_PF = BAR_SF + 1;
-    static constexpr int BAR_AF = BAR_PF + 1;
+    static constexpr int BAR_SF = BAR_RE + SLOTS;  // [2]: a half's S and dP written
+    static constexpr int BAR_PF = BAR_SF + 2;      // [2]: a half's P / dS written back
+    static constexpr int BAR_AF = BAR_PF + 2;
     static constexpr int BAR_AE = BAR_AF + 1;
     static constexpr int BAR_LD = BAR_AE + 1;  // [2]: a step's LSE and D staged (dK/dV kernel)
     static constexpr int BAR_DONE = BAR_LD + 2;
@@ -249,32 +250,60 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
                                         int units, const BwdArgs &a, const WaitGuard &g) {
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
-    constexpr uint32_t idesc_sq = mma_idesc_f16(G::BT, G::BT, BF16, false, false);  // 128x128 tiles
-    constexpr uint32_t idesc_acc = mma_idesc_f16(G::BT, D, BF16, false, true);      // ... x d, B MN-major
+    constexpr uint32_t idesc_half = mma_idesc_f16(G::BT, G::HN, BF16, false, false);  // 128 x HN
+    constexpr uint32_t idesc_acc = mma_idesc_f16(G::BT, D, BF16, false, true);      // 128 x d, B MN-major
     // K-major and MN-major descriptors of the fixed tiles and of ring slot 0
     const uint64_t fix_k = smem_desc(sbase + G::OFF_FIX, 16, G::SBO, G::LAYOUT);
     const uint64_t ring_k = smem_desc(sbase + G::OFF_RING, 16, G::SBO, G::LAYOUT);
     const uint64_t ring_mn = smem_desc(sbase + G::OFF_RING, G::PANEL_BYTES, G::SBO, G::LAYOUT);
     constexpr uint32_t tile16 = G::TILE_BYTES >> 4;
+    // HN rows into a tile: a whole number of swizzle atoms (8 rows each)
+    constexpr uint32_t half16 = (G::HN * G::ROW_BYTES) >> 4;
 
-    // A (K-major, fixed or ring) times B (K-major) over the head dim: a 128 x 128 tile.
-    auto mma_kk = [&](uint32_t dst, uint64_t adesc, uint64_t bdesc) {
+    // Half h of a step's S and dP: the fixed tiles (A, 128 rows) times rows
+    // [h HN, (h+1) HN) of the streamed pair (B, K-major), over the head dim.
+    auto issue_sdp = [&](int sa, int sb, int h) {
+        const uint64_t ba = ring_k + sa * tile16 + h * half16;
+        const uint64_t bb = ring_k + sb * tile16 + h * half16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int p = (kk * 16) / G::PANEL_ELEMS;
             const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
             const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
-            mma_ss(dst, adesc + o16, bdesc + o16, idesc_sq, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + G::T_S + h * G::HN, fix_k + o16, ba + o16, idesc_half, kk > 0 ? 1u : 0u);
         }
-    };
-    // acc (+)= A[TMEM, 128 rows x 128] * B[128 x d, MN-major], 16 rows of B per MMA
-    auto mma_acc = [&](uint32_t dst, uint32_t a_tmem, uint64_t bdesc_mn, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < G::BT / 16; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int p = (kk * 16) / G::PANEL_ELEMS;
+            const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
+            const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
+            mma_ss(tmem + G::T_P + h * G::HN, fix_k + tile16 + o16, bb + o16, idesc_half,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(G::BAR_SF + h));
+    };
+    // acc (+)= A[TMEM: 128 rows x HN, 16-bit, packed in HN/2 columns] times
+    // B[HN rows x d, MN-major], 16 rows of B per MMA
+    auto mma_acc_half = [&](uint32_t dst, uint32_t a_tmem, uint64_t bdesc_mn, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < G::HN / 16; ++kk)
             mma_ts(dst, a_tmem + kk * 8, bdesc_mn + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_acc,
                    (!first || kk > 0) ? 1u : 0u);
     };
+    // ring slots of global step gs, waited for until loaded
+    auto wait_ring = [&](int gs, int &sa, int &sb) {
+        const int na = 2 * gs, nb = na + 1;
+        sa = na % G::SLOTS;
+        sb = nb % G::SLOTS;
+        return mbar_wait(bar(G::BAR_RF + sa), (na / G::SLOTS) & 1, g, 5) &&
+               mbar_wait(bar(G::BAR_RF + sb), (nb / G::SLOTS) & 1, g, 6);
+    };
 
+    // Software pipeline over half steps. For half h of step j the issuer
+    // waits for the warps' P / dS of (j, h), queues the accumulation of
+    // (j, h) and then S / dP of (j + 1, h) into the same columns (the tensor
+    // core runs in order, so the accumulation has read them first). The
+    // tensor core works on one half while the warps work on the other.
     int it_u = 0, base = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
@@ -286,50 +315,64 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
             mma_commit(bar(G::BAR_AF));
             continue;
         }
-        for (int j = 0; j < count; ++j) {
-            const int na = 2 * (base + j), nb = na + 1;
-            const int sa = na % G::SLOTS, sb = nb % G::SLOTS;
-            if (!mbar_wait(bar(G::BAR_RF + sa), (na / G::SLOTS) & 1, g, 5) ||
-                !mbar_wait(bar(G::BAR_RF + sb), (nb / G::SLOTS) & 1, g, 6)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if constexpr (MODE == kBwdDQ) {
-                // S = Q K_j^T, dP = dO V_j^T
-                mma_kk(tmem + G::T_S, fix_k, ring_k + sa * tile16);
-                mma_kk(tmem + G::T_P, fix_k + tile16, ring_k + sb * tile16);
-            } else {
-                // S^T = K Q_i^T, dP^T = V dO_i^T
-                mma_kk(tmem + G::T_S, fix_k, ring_k + sa * tile16);
-                mma_kk(tmem + G::T_P, fix_k + tile16, ring_k + sb * tile16);
-            }
-            mma_commit(bar(G::BAR_SF));
-            // the warps turn the tiles into 16-bit P / dS in place
-            if (!mbar_wait(bar(G::BAR_PF), (base + j) & 1, g, 8)) {
-                ok = false;
-                break;
-            }
-            // The first accumulation of a unit overwrites the accumulators: the
-            // previous unit's epilogue must have read them out.
-            if (j == 0 && !mbar_wait(bar(G::BAR_AE), (it_u & 1) ^ 1, g, 7)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if constexpr (MODE == kBwdDQ) {
-                mma_acc(tmem + G::T_A0, tmem + G::T_S, ring_mn + sa * tile16, j == 0);  // dQ += dS K_j
-            } else {
-                mma_acc(tmem + G::T_A0, tmem + G::T_S, ring_mn + sb * tile16, j == 0);  // dV += P^T dO_i
-                mma_acc(tmem + G::T_A1, tmem + G::T_P, ring_mn + sa * tile16, j == 0);  // dK += dS^T Q_i
-            }
-            mma_commit(bar(G::BAR_RE + sa));
-            mma_commit(bar(G::BAR_RE + sb));
-            if (j == count - 1) {
-                mma_commit(bar(G::BAR_FE));
-                mma_commit(bar(G::BAR_AF));
-            }
+        int sa = 0, sb = 0;
+        if (!wait_ring(base, sa, sb)) {
+            ok = false;
+            break;
         }
+        tc_fence_after();
+        issue_sdp(sa, sb, 0);
+        issue_sdp(sa, sb, 1);
+        for (int j = 0; ok && j < count; ++j) {
+            const int gs = base + j;
+            int na = 0, nb = 0;  // ring slots of step j + 1
+            for (int h = 0; h < 2; ++h) {
+                if (!mbar_wait(bar(G::BAR_PF + h), gs & 1, g, 8)) {
+                    ok = false;
+                    break;
+                }
+                // The first accumulation of a unit overwrites the accumulators:
+                // the previous unit's epilogue must have read them out.
+                if (j == 0 && h == 0 && !mbar_wait(bar(G::BAR_AE), (it_u & 1) ^ 1, g, 7)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const bool first_acc = j == 0 && h == 0;
+                const uint32_t col = h * G::HN;
+                if constexpr (MODE == kBwdDQ) {
+                    // dQ += dS K_j (rows of K_j in this half)
+                    mma_acc_half(tmem + G::T_A0, tmem + G::T_S + col, ring_mn + sa * tile16 + h * half16,
+                                 first_acc);
+                } else {
+                    // dV += P^T dO_i, dK += dS^T Q_i (query rows of this half)
+                    mma_acc_half(tmem + G::T_A0, tmem + G::T_S + col, ring_mn + sb * tile16 + h * half16,
+                                 first_acc);
+                    mma_acc_half(tmem + G::T_A1, tmem + G::T_P + col, ring_mn + sa * tile16 + h * half16,
+                                 first_acc);
+                }
+                if (h == 1) {  // step j's streamed tiles are read for the last time
+                    mma_commit(bar(G::BAR_RE + sa));
+                    mma_commit(bar(G::BAR_RE + sb));
+                }
+                if (j + 1 < count) {
+                    if (h == 0) {
+                        if (!wait_ring(gs + 1, na, nb)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    issue_sdp(na, nb, h);
+                }
+            }
+            if (!ok) break;
+            sa = na;
+            sb = nb;
+        }
+        if (!ok) break;
+        mma_commit(bar(G::BAR_FE));
+        mma_commit(bar(G::BAR_AF));
         base += count;
     }
     mma_commit(bar(G::BAR_DONE));
@@ -407,75 +450,81 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                 if (!__all_sync(0xffffffffu, okl)) return;
                 ldbuf = buf;
             }
-            const bool ok = mbar_wait(bar(G::BAR_SF), step & 1, g, 13);
-            if (!__all_sync(0xffffffffu, ok)) return;
-            tc_fence_after();
-            if constexpr (MODE == kBwdDQ) {
-                // row = query row; columns = keys j*128 .. : P = 2^(s c - lse2),
-                // dS = P (dP - D); keys past sk (TMA zero fill) take no part.
-                // (causal: the row's own last visible key)
-                const int kv = (CAUSAL ? min(a.sk, grow + a.sk - a.sq + 1) : a.sk) - tj * G::BT;
+            // the score tile in two halves of HN columns, as the MMAs make them
+            for (int h = 0; h < 2; ++h) {
+                const bool ok = mbar_wait(bar(G::BAR_SF + h), step & 1, g, 13);
+                if (!__all_sync(0xffffffffu, ok)) return;
+                tc_fence_after();
+                const int hc = h * G::HN;  // first column of the half
+                if constexpr (MODE == kBwdDQ) {
+                    // row = query row; columns = keys tj*128 + hc .. : P = 2^(s c - lse2),
+                    // dS = P (dP - D); keys past sk (TMA zero fill) take no part.
+                    // (causal: the row's own last visible key)
+                    const int kv = (CAUSAL ? min(a.sk, grow + a.sk - a.sq + 1) : a.sk) - tj * G::BT - hc;
 #pragma unroll
-                for (int c0 = 0; c0 < G::BT; c0 += 32) {
-                    uint32_t sv[32], pv[32];
-                    tmem_ld32(tmem + lanes + G::T_S + c0, sv);
-                    tmem_ld32(tmem + lanes + G::T_P + c0, pv);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+                    for (int c0 = 0; c0 < G::HN; c0 += 32) {
+                        uint32_t sv[32], pv[32];
+                        tmem_ld32(tmem + lanes + G::T_S + hc + c0, sv);
+                        tmem_ld32(tmem + lanes + G::T_P + hc + c0, pv);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int k = c0 + 2 * i;
-                        const float p0 = k < kv ? fast_exp2(__uint_as_float(sv[2 * i]) * c - lse2) : 0.f;
-                        const float p1 =
-                            k + 1 < kv ? fast_exp2(__uint_as_float(sv[2 * i + 1]) * c - lse2) : 0.f;
-                        pk[i] = pack2b<BF16>(p0 * (__uint_as_float(pv[2 * i]) - drow),
-                                             p1 * (__uint_as_float(pv[2 * i + 1]) - drow));
-                    }
-                    // dS of keys c0 .. c0+31 into columns c0/2 .. c0/2+15, all read already
-                    tmem_st16(tmem + lanes + G::T_S + c0 / 2, pk);
-                }
-            } else {
-                // row = key row; columns = query rows j*128 .. with their own
-                // LSE and D, staged for the step in shared memory (query rows
-                // past sq get LSE = +inf, hence P = 0, and D = 0).
-                const float4 *ld4 = reinterpret_cast<const float4 *>(ldbuf);
-                // causal: this key row is seen by query columns >= cmin
-                const int cmin = CAUSAL ? grow - (a.sk - a.sq) - tj * G::BT : -1;
-#pragma unroll
-                for (int c0 = 0; c0 < G::BT; c0 += 32) {
-                    uint32_t sv[32], pv[32];
-                    tmem_ld32(tmem + lanes + G::T_S + c0, sv);
-                    tmem_ld32(tmem + lanes + G::T_P + c0, pv);
-                    tmem_wait_ld();
-                    uint32_t pp[16], pd[16];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {  // four columns per shared-memory read
-                        const float4 l4 = ld4[(c0 >> 2) + q];
-                        const float4 d4 = ld4[(G::BT >> 2) + (c0 >> 2) + q];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pr[4], dr[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 4 * q + e;
-                            pr[e] = fast_exp2(__uint_as_float(sv[i]) * c - lv[e]);
-                            if constexpr (CAUSAL) pr[e] = (c0 + i >= cmin) ? pr[e] : 0.f;
-                            dr[e] = pr[e] * (__uint_as_float(pv[i]) - dv[e]);
+                        for (int i = 0; i < 16; ++i) {
+                            const int k = c0 + 2 * i;
+                            const float p0 =
+                                k < kv ? fast_exp2(__uint_as_float(sv[2 * i]) * c - lse2) : 0.f;
+                            const float p1 =
+                                k + 1 < kv ? fast_exp2(__uint_as_float(sv[2 * i + 1]) * c - lse2) : 0.f;
+                            pk[i] = pack2b<BF16>(p0 * (__uint_as_float(pv[2 * i]) - drow),
+                                                 p1 * (__uint_as_float(pv[2 * i + 1]) - drow));
                         }
-                        pp[2 * q] = pack2b<BF16>(pr[0], pr[1]);
-                        pp[2 * q + 1] = pack2b<BF16>(pr[2], pr[3]);
-                        pd[2 * q] = pack2b<BF16>(dr[0], dr[1]);
-                        pd[2 * q + 1] = pack2b<BF16>(dr[2], dr[3]);
+                        // dS of the half's keys c0 .. c0+31 into its columns c0/2 .. c0/2+15
+                        tmem_st16(tmem + lanes + G::T_S + hc + c0 / 2, pk);
                     }
-                    // P^T and dS^T of columns c0 .. c0+31 into columns c0/2 .. c0/2+15
-                    tmem_st16(tmem + lanes + G::T_S + c0 / 2, pp);
-                    tmem_st16(tmem + lanes + G::T_P + c0 / 2, pd);
+                } else {
+                    // row = key row; columns = query rows tj*128 + hc .. with their
+                    // own LSE and D, staged for the step in shared memory (query rows
+                    // past sq get LSE = +inf, hence P = 0, and D = 0).
+                    const float4 *ld4 = reinterpret_cast<const float4 *>(ldbuf);
+                    // causal: this key row is seen by the tile's query columns >= cmin
+                    const int cmin = CAUSAL ? grow - (a.sk - a.sq) - tj * G::BT : -1;
+#pragma unroll
+                    for (int c0 = 0; c0 < G::HN; c0 += 32) {
+                        uint32_t sv[32], pv[32];
+                        tmem_ld32(tmem + lanes + G::T_S + hc + c0, sv);
+                        tmem_ld32(tmem + lanes + G::T_P + hc + c0, pv);
+                        tmem_wait_ld();
+                        uint32_t pp[16], pd[16];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {  // four columns per shared-memory read
+                            const float4 l4 = ld4[((hc + c0) >> 2) + q];
+                            const float4 d4 = ld4[(G::BT >> 2) + ((hc + c0) >> 2) + q];
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                            float pr[4], dr[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 4 * q + e;
+                                pr[e] = fast_exp2(__uint_as_float(sv[i]) * c - lv[e]);
+                                if constexpr (CAUSAL) pr[e] = (hc + c0 + i >= cmin) ? pr[e] : 0.f;
+                                dr[e] = pr[e] * (__uint_as_float(pv[i]) - dv[e]);
+                            }
+                            pp[2 * q] = pack2b<BF16>(pr[0], pr[1]);
+                            pp[2 * q + 1] = pack2b<BF16>(pr[2], pr[3]);
+                            pd[2 * q] = pack2b<BF16>(dr[0], dr[1]);
+                            pd[2 * q + 1] = pack2b<BF16>(dr[2], dr[3]);
+                        }
+                        // P^T and dS^T of the half's columns c0 .. c0+31 into its
+                        // columns c0/2 .. c0/2+15
+                        tmem_st16(tmem + lanes + G::T_S + hc + c0 / 2, pp);
+                        tmem_st16(tmem + lanes + G::T_P + hc + c0 / 2, pd);
+                    }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(G::BAR_PF + h));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(G::BAR_PF));
         }
 
         // ---------------------------------------------------- epilogue
@@ -527,7 +576,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i)
-            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_AE || i == G::BAR_LD || i == G::BAR_LD + 1)
+            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_PF + 1 || i == G::BAR_AE ||
+                               i == G::BAR_LD || i == G::BAR_LD + 1)
                                   ? 4u    // one per compute warp
                                   : 1u);
         *abort_flag = 0u;

@@ -60,6 +60,9 @@ struct BwdGeom {
     static constexpr uint32_t SBO = 8 * ROW_BYTES;
     static constexpr int TMEM_COLS = 512;
     static constexpr int T_S = 0, T_P = 128, T_A0 = 256, T_A1 = 384;
+    // dQ kernel: the fixed Q and dO tiles as 16-bit MMA A operands in TMEM
+    static constexpr int T_Q = 384, T_DO = T_Q + D / 2;
+    static_assert(T_DO + D / 2 <= TMEM_COLS, "TMEM budget");
 
     static constexpr int OFF_FIX = 0;                       // the unit's two fixed tiles
     static constexpr int OFF_RING = 2 * TILE_BYTES;
@@ -262,6 +265,9 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
 
     // Half h of a step's S and dP: the fixed tiles (A, 128 rows) times rows
     // [h HN, (h+1) HN) of the streamed pair (B, K-major), over the head dim.
+    // (dQ kernel: A = Q and dO from TMEM, copied there once per unit, so
+    // that only B is read from shared memory; dK/dV kernel: A = K and V from
+    // shared memory, TMEM being full.)
     auto issue_sdp = [&](int sa, int sb, int h) {
         const uint64_t ba = ring_k + sa * tile16 + h * half16;
         const uint64_t bb = ring_k + sb * tile16 + h * half16;
@@ -270,15 +276,23 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
             const int p = (kk * 16) / G::PANEL_ELEMS;
             const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
             const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
-            mma_ss(tmem + G::T_S + h * G::HN, fix_k + o16, ba + o16, idesc_half, kk > 0 ? 1u : 0u);
+            if constexpr (MODE == kBwdDQ)
+                mma_ts(tmem + G::T_S + h * G::HN, tmem + G::T_Q + kk * 8, ba + o16, idesc_half,
+                       kk > 0 ? 1u : 0u);
+            else
+                mma_ss(tmem + G::T_S + h * G::HN, fix_k + o16, ba + o16, idesc_half, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int p = (kk * 16) / G::PANEL_ELEMS;
             const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
             const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
-            mma_ss(tmem + G::T_P + h * G::HN, fix_k + tile16 + o16, bb + o16, idesc_half,
-                   kk > 0 ? 1u : 0u);
+            if constexpr (MODE == kBwdDQ)
+                mma_ts(tmem + G::T_P + h * G::HN, tmem + G::T_DO + kk * 8, bb + o16, idesc_half,
+                       kk > 0 ? 1u : 0u);
+            else
+                mma_ss(tmem + G::T_P + h * G::HN, fix_k + tile16 + o16, bb + o16, idesc_half,
+                       kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(G::BAR_SF + h));
     };
@@ -314,6 +328,21 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
             mma_commit(bar(G::BAR_FE));
             mma_commit(bar(G::BAR_AF));
             continue;
+        }
+        if constexpr (MODE == kBwdDQ) {
+            // Q and dO into TMEM, 16 head-dim columns per copy, after the last
+            // S / dP MMAs of the previous unit (same thread, in order); then
+            // their shared-memory tiles are free for the next unit's loads.
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int p = (kk * 16) / G::PANEL_ELEMS;
+                const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
+                const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
+                tmem_cp_128x256b(tmem + G::T_Q + kk * 8, fix_k + o16);
+                tmem_cp_128x256b(tmem + G::T_DO + kk * 8, fix_k + tile16 + o16);
+            }
+            mma_commit(bar(G::BAR_FE));
         }
         int sa = 0, sb = 0;
         if (!wait_ring(base, sa, sb)) {
@@ -371,7 +400,7 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
             sb = nb;
         }
         if (!ok) break;
-        mma_commit(bar(G::BAR_FE));
+        if constexpr (MODE == kBwdDKV) mma_commit(bar(G::BAR_FE));
         mma_commit(bar(G::BAR_AF));
         base += count;
     }

@@ -204,6 +204,13 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]
+// Copy a 128-row x 256-bit matrix (one K = 16 slice of a 16-bit operand)
+// from shared memory, given by its matrix descriptor, into TMEM lanes 0-127,
+// 8 columns from taddr. Ordered with the issuing thread's tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(

@@ -500,10 +500,10 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int k = c0 + 2 * i;
-                            const float p0 =
-                                k < kv ? fast_exp2(__uint_as_float(sv[2 * i]) * c - lse2) : 0.f;
-                            const float p1 =
-                                k + 1 < kv ? fast_exp2(__uint_as_float(sv[2 * i + 1]) * c - lse2) : 0.f;
+                            float p0 = fast_exp2(__uint_as_float(sv[2 * i]) * c - lse2);
+                            float p1 = fast_exp2(__uint_as_float(sv[2 * i + 1]) * c - lse2);
+                            p0 = k < kv ? p0 : 0.f;
+                            p1 = k + 1 < kv ? p1 : 0.f;
                             pk[i] = pack2b<BF16>(p0 * (__uint_as_float(pv[2 * i]) - drow),
                                                  p1 * (__uint_as_float(pv[2 * i + 1]) - drow));
                         }

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "exattn.h"
 #include "internal.h"
@@ -81,6 +82,15 @@ struct DeviceState {
     int num_sms = 0;
     // copy streams of the host-buffer forward, made on first use
     cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
+    // arrival counters of the split decode's in-kernel reduce, one array per
+    // stream (calls on one stream are ordered, so its counters are all zero
+    // whenever a call starts)
+    struct Arrivals {
+        cudaStream_t stream;
+        uint32_t *p;
+        int64_t n;
+    };
+    std::vector<Arrivals> arrivals;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -131,6 +141,42 @@ attn_status_t copy_streams(DeviceState *ds) {
         return ATTN_ERR_CUDA;
     }
     return ATTN_OK;
+}
+
+// At least n zeroed arrival counters for `stream` (grown stream-ordered,
+// on that stream). nullptr, and the combine kernel, while the stream is being
+// captured into a graph: replays of a graph could run concurrently.
+uint32_t *arrival_counters(DeviceState *ds, cudaStream_t stream, int64_t n) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState::Arrivals *e = nullptr;
+    for (auto &x : ds->arrivals)
+        if (x.stream == stream) e = &x;
+    if (e != nullptr && e->n >= n) return e->p;
+    const int64_t cap = n < 1024 ? 1024 : n;
+    uint32_t *p = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&p), cap * sizeof(uint32_t), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cudaMemsetAsync(p, 0, cap * sizeof(uint32_t), stream) != cudaSuccess) {
+        cudaFreeAsync(p, stream);
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (e != nullptr) {
+        cudaFreeAsync(e->p, stream);  // after the work already queued on it
+        e->p = p;
+        e->n = cap;
+    } else {
+        ds->arrivals.push_back(DeviceState::Arrivals{stream, p, cap});
+    }
+    return p;
 }
 
 CUtensorMapSwizzle fwd_swizzle(int d) {
@@ -541,8 +587,9 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
     void *ws = nullptr;
     if ((st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
         return st;
+    a.arrivals = arrival_counters(ds, stream, static_cast<int64_t>(b) * cdiv(sq, dec_rows_per_cta(sq)) * h);
     cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && a.arrivals == nullptr)
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
@@ -630,8 +677,9 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     void *ws = nullptr;
     if ((st = alloc_partials(splits, b, 1, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
         return st;
+    a.arrivals = arrival_counters(ds, stream, static_cast<int64_t>(b) * h);
     cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && a.arrivals == nullptr)
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, 1, h, a.splits, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
@@ -662,11 +710,14 @@ attn_status_t attn_get_device_status(cudaStream_t stream) {
 void attn_release_workspace(void) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return;
-    cudaMemPool_t pool;
-    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
-        cudaDeviceSynchronize();
-        cudaMemPoolTrimTo(pool, 0);
+    cudaDeviceSynchronize();
+    if (dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (auto &x : g_dev[dev].arrivals) cudaFree(x.p);
+        g_dev[dev].arrivals.clear();
     }
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) cudaMemPoolTrimTo(pool, 0);
 }
 
 }  // extern "C"

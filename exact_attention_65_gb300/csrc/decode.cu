@@ -6,11 +6,15 @@
 // online softmax over it, writing its own O_i and LSE_i. With a single
 // split it writes the final O and LSE directly.
 //
-// Stage 2 (combine_kernel): the reduce stated in the flash-decoding issue
-// ("where is flash decoding second stage (reduce) code?"), with the max
-// split LSE taken out first:
+// Stage 2: the reduce stated in the flash-decoding issue ("where is flash
+// decoding second stage (reduce) code?"), with the max split LSE taken out
+// first:
 //     M = max_i LSE_i, LSE = M + ln sum_i exp(LSE_i - M),
 //     O = sum_i exp(LSE_i - LSE) * O_i.
+// It runs in the split kernel itself: each split CTA counts its arrival on
+// a per-(batch, query block, head) counter after its partials are written,
+// and the one that arrives last reduces them (no CTA waits for another). A
+// separate combine_kernel does the same when no counters are given.
 //
 // Decode does about one multiply-add per byte of K and V, so it is bound by
 // HBM bandwidth, not by math (the same issue: its speed is close to a
@@ -297,6 +301,105 @@ __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty e
     }
 }
 
+// Many splits: lane i holds LSE_i of the splits i, i+32, ...; every load is
+// independent of the ones before it, so the warp keeps many in flight
+// instead of paying one memory latency per split. Returns LSE; acc gets O.
+template <int D>
+__device__ __forceinline__ float combine_many(const float *__restrict__ lse_part,
+                                              const float *__restrict__ src, int64_t lse_idx,
+                                              int64_t lse_stride, int64_t o_stride, int splits,
+                                              int lane, float (&acc)[D >= 32 ? D / 32 : 1]) {
+    constexpr int PER = D >= 32 ? D / 32 : 1;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float mx = -INFINITY;
+#pragma unroll 4
+    for (int i = lane; i < splits; i += 32) mx = fmaxf(mx, __ldcg(lse_part + i * lse_stride + lse_idx));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float tot = 0.f;
+#pragma unroll 4
+    for (int i = lane; i < splits; i += 32) {
+        const float li = __ldcg(lse_part + i * lse_stride + lse_idx);
+        tot += (li == -INFINITY) ? 0.f : fast_exp2((li - mx) * kLog2e);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    const float L = mx + __logf(tot);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int i0 = 0; i0 < splits; i0 += 32) {
+        // weight of split i0 + lane (0 for an empty split or past the end)
+        const float li =
+            (i0 + lane < splits) ? __ldcg(lse_part + (i0 + lane) * lse_stride + lse_idx) : -INFINITY;
+        const float wl = (li == -INFINITY) ? 0.f : fast_exp2((li - L) * kLog2e);
+        const int n = min(32, splits - i0);
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
+#pragma unroll
+            for (int e = 0; e < PER; ++e)
+                acc[e] = fmaf(w, __ldcg(src + (i0 + j) * o_stride + 32 * e), acc[e]);
+        }
+    }
+    return L;
+}
+
+// The reduce of one output row (batch, query row, head) by one warp. The
+// partials are read through L2 only (other CTAs wrote them).
+template <int D, bool BF16>
+__device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
+                                            const float *__restrict__ lse_part, void *o, float *lse,
+                                            int b, int sq, int h, int splits, int batch, int qrow,
+                                            int head, int lane) {
+    constexpr int PER = D >= 32 ? D / 32 : 1;
+    const int64_t rows = static_cast<int64_t>(b) * sq * h;
+    const int64_t r = (static_cast<int64_t>(batch) * sq + qrow) * h + head;
+    const int64_t lse_idx = (static_cast<int64_t>(batch) * h + head) * sq + qrow;
+    const int64_t lse_stride = static_cast<int64_t>(b) * h * sq;
+    const int64_t o_stride = rows * D;
+    constexpr float kLog2e = 1.4426950408889634f;
+
+    const bool active = D >= 32 || lane < D;
+    const float *src = o_part + r * D + (active ? lane : 0);
+    float acc[PER];
+    float L;
+    constexpr int kFew = 16;
+    if (splits <= kFew) {
+        // Few splits: lane i holds LSE_i, and every partial of the row is
+        // requested at once, so the reduce waits for one memory latency.
+        const float li = lane < splits ? __ldcg(lse_part + lane * lse_stride + lse_idx) : -INFINITY;
+        float ov[kFew][PER];
+#pragma unroll
+        for (int i = 0; i < kFew; ++i)
+#pragma unroll
+            for (int e = 0; e < PER; ++e) ov[i][e] = i < splits ? __ldcg(src + i * o_stride + 32 * e) : 0.f;
+        float mx = li;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float tot = (li == -INFINITY) ? 0.f : fast_exp2((li - mx) * kLog2e);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        L = mx + __logf(tot);
+        const float wl = (li == -INFINITY) ? 0.f : fast_exp2((li - L) * kLog2e);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < kFew; ++i) {
+            const float w = __shfl_sync(0xffffffffu, wl, i);  // 0 past the last split
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, ov[i][e], acc[e]);
+        }
+    } else {
+        L = combine_many<D>(lse_part, src, lse_idx, lse_stride, o_stride, splits, lane, acc);
+    }
+    if (active) {
+        uint16_t *dst = reinterpret_cast<uint16_t *>(o) + r * D;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = to_elem<BF16>(acc[e]);
+    }
+    if (lane == 0) lse[lse_idx] = L;
+}
+
 template <int D, int QR, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(DecGeom<D>::THREADS)
     decode_split_kernel(const __grid_constant__ CUtensorMap tk,
@@ -379,6 +482,30 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
                                     blk1, row_end, a, g);
     }
     __syncthreads();
+
+    // ---------------------------------------- reduce by the last split
+    // Every CTA counts its arrival once its partials are written (also after
+    // an abort, so that the counter still comes back to zero). The fence
+    // orders the CTA's partial stores, which thread 0 has observed through
+    // the barrier, before the count; the last arriver fences again before it
+    // reads the others' partials.
+    if (a.splits > 1 && a.arrivals != nullptr) {
+        volatile uint32_t *is_last = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 8);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            uint32_t *cnt = a.arrivals + static_cast<int64_t>(blockIdx.z) * a.h + head;
+            const bool last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(a.splits - 1);
+            if (last) {
+                atomicExch(cnt, 0u);  // every split has counted: ready for the next call
+                __threadfence();
+            }
+            *is_last = last ? 1u : 0u;
+        }
+        __syncthreads();
+        if (*is_last && warp < nq)
+            combine_row<D, BF16>(a.o_part, a.lse_part, a.o, a.lse, a.b, a.sq, a.h, a.splits, batch,
+                                 q0 + warp, head, lane);
+    }
 }
 
 // One warp per output row (batch, query row, head).
@@ -386,7 +513,6 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(128)
     combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, void *o,
                    float *lse, int b, int sq, int h, int splits) {
-    constexpr int PER = D >= 32 ? D / 32 : 1;
     const int lane = threadIdx.x & 31;
     const int64_t rows = static_cast<int64_t>(b) * sq * h;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
@@ -394,58 +520,10 @@ __global__ void __launch_bounds__(128)
     const int head = static_cast<int>(r % h);
     const int qrow = static_cast<int>((r / h) % sq);
     const int batch = static_cast<int>(r / (static_cast<int64_t>(h) * sq));
-    const int64_t lse_idx = (static_cast<int64_t>(batch) * h + head) * sq + qrow;
-    const int64_t lse_stride = static_cast<int64_t>(b) * h * sq;
-    const int64_t o_stride = rows * D;
-    constexpr float kLog2e = 1.4426950408889634f;
-
     // The partials come from the split kernel, which may still be draining
     // when this grid starts (programmatic dependent launch).
     griddep_wait();
-
-    // Lane i holds LSE_i of the splits i, i+32, ... Every load below is
-    // independent of the ones before it, so the warp keeps many in flight
-    // instead of paying one memory latency per split.
-    float mx = -INFINITY;
-#pragma unroll 4
-    for (int i = lane; i < splits; i += 32) mx = fmaxf(mx, lse_part[i * lse_stride + lse_idx]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float tot = 0.f;
-#pragma unroll 4
-    for (int i = lane; i < splits; i += 32) {
-        const float li = lse_part[i * lse_stride + lse_idx];
-        tot += (li == -INFINITY) ? 0.f : fast_exp2((li - mx) * kLog2e);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    const float L = mx + __logf(tot);
-
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    const bool active = D >= 32 || lane < D;
-    const float *src = o_part + r * D + (active ? lane : 0);
-    for (int i0 = 0; i0 < splits; i0 += 32) {
-        // weight of split i0 + lane (0 for an empty split or past the end)
-        const float li = (i0 + lane < splits) ? lse_part[(i0 + lane) * lse_stride + lse_idx]
-                                              : -INFINITY;
-        const float wl = (li == -INFINITY) ? 0.f : fast_exp2((li - L) * kLog2e);
-        const int n = min(32, splits - i0);
-#pragma unroll 8
-        for (int j = 0; j < n; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wl, j);
-#pragma unroll
-            for (int e = 0; e < PER; ++e)
-                acc[e] = fmaf(w, src[(i0 + j) * o_stride + 32 * e], acc[e]);
-        }
-    }
-    if (active) {
-        uint16_t *dst = reinterpret_cast<uint16_t *>(o) + r * D;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = to_elem<BF16>(acc[e]);
-    }
-    if (lane == 0) lse[lse_idx] = L;
+    combine_row<D, BF16>(o_part, lse_part, o, lse, b, sq, h, splits, batch, qrow, head, lane);
 }
 
 template <int D, int QR, bool BF16, bool PAGED>

@@ -102,6 +102,11 @@ struct DecodeArgs {
     int page_size = 0;
     int max_pages = 0;
     int num_pages = 0;
+    // splits > 1: one arrival counter per (batch, query block, head), zero
+    // between calls; the split that arrives last reduces the partials of its
+    // rows and sets the counter back to zero. nullptr: the combine kernel
+    // reduces instead.
+    uint32_t *arrivals = nullptr;
 };
 
 cudaError_t launch_decode(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,

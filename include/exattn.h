@@ -133,8 +133,13 @@ attn_status_t attn_bwd_causal(const void *q, const void *k, const void *v, const
  * Split-KV decode, bf16 q/k/v/o ("where is flash decoding second stage
  * (reduce) code?" issue). seqlen_k is cut into num_splits ranges of whole
  * key blocks; split i writes its own O_i and LSE_i (fp32, library
- * workspace), and a reduce kernel forms, with the max LSE taken out first,
+ * workspace), and the reduce forms, with the max LSE taken out first,
  *     LSE = log(sum_i exp(LSE_i)),   O = sum_i exp(LSE_i - LSE) * O_i.
+ * With sq == 1 the reduce runs inside the split kernel: the split of a
+ * (batch, head) that finishes last reduces it, found through a small array
+ * of arrival counters the library keeps per stream (zero between calls;
+ * released by attn_release_workspace). While the stream is being captured
+ * into a graph, and with sq > 1, a second kernel reduces instead.
  * num_splits = 0 lets attn_decode_num_splits() choose; a positive value is
  * clamped to the number of key blocks. With one split the first kernel
  * writes O and LSE directly and no workspace is used. Any sq >= 1 is

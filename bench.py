@@ -6,8 +6,8 @@ input, on one GPU:
   * forward: b4 s512 h32 d128 bf16 (the problem timed in "Why
     FlashAttention is fast"), O and LSE, one kernel;
   * split-KV decode: b1 h16 sk32768 d128 bf16 (the small-batch decode of
-    the flash-decoding issue), heuristic split count, split kernel plus the
-    LSE-combine kernel.
+    the flash-decoding issue), heuristic split count, one split kernel whose
+    last-finishing split of each head does the LSE combine.
 Headline: forward TFLOP/s (4*b*h*sq*sk*d per call); decode is reported as
 HBM GB/s beside it. Inputs are resident in HBM when the timed region starts;
 L2 is flushed (a 512 MiB write) before every timed kernel. Each kernel is
@@ -342,11 +342,11 @@ def run_ours(args):
                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": round(per_rank_dec_gbs / peaks["hbm_gbs"], 4),
                             "traffic": ncu_traffic("decode_b1"), "peak_source": peak_src,
-                            "kernel": "decode_split_kernel<128, 1, bf16> + combine_kernel",
+                            "kernel": "decode_split_kernel<128, 1, bf16> (combine in-kernel)",
                             "algorithmic_per_launch": DEC.io_bytes},
         "e2e": {"value": round(e2e_tflops, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(times["e2e_ms"], 4)},
-        "gpu_launches": args.steps * (1 + (2 if splits > 1 else 1)),
+        "gpu_launches": args.steps * 2,  # the forward kernel and the split decode kernel
         "clocks": clocks,
         "cpu_baseline": cpu,
         "extras": extras,

@@ -253,7 +253,13 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
                                         int units, const BwdArgs &a, const WaitGuard &g) {
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
-    constexpr uint32_t idesc_half = mma_idesc_f16(G::BT, G::HN, BF16, false, false);  // 128 x HN
+    // Width of the S / dP MMAs. A 128 x 64 MMA takes about as long on the
+    // tensor core as a 128 x 128 one, so the key-tile kernel (four products
+    // per step, tensor-bound) makes S and dP whole; the query-tile kernel
+    // makes them in halves, which lets the tensor core work on one half while
+    // the warps work on the other.
+    constexpr bool kFull = MODE == kBwdDKV;
+    constexpr uint32_t idesc_half = mma_idesc_f16(G::BT, kFull ? G::BT : G::HN, BF16, false, false);
     constexpr uint32_t idesc_acc = mma_idesc_f16(G::BT, D, BF16, false, true);      // 128 x d, B MN-major
     // K-major and MN-major descriptors of the fixed tiles and of ring slot 0
     const uint64_t fix_k = smem_desc(sbase + G::OFF_FIX, 16, G::SBO, G::LAYOUT);
@@ -263,24 +269,27 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
     // HN rows into a tile: a whole number of swizzle atoms (8 rows each)
     constexpr uint32_t half16 = (G::HN * G::ROW_BYTES) >> 4;
 
-    // Half h of a step's S and dP: the fixed tiles (A, 128 rows) times rows
-    // [h HN, (h+1) HN) of the streamed pair (B, K-major), over the head dim.
+    // Half h of a step's S and dP (or both halves at once): the fixed tiles
+    // (A, 128 rows) times rows [h HN, (h+1) HN) of the streamed pair (B,
+    // K-major), over the head dim.
     // (dQ kernel: A = Q and dO from TMEM, copied there once per unit, so
     // that only B is read from shared memory; dK/dV kernel: A = K and V from
     // shared memory, TMEM being full.)
     auto issue_sdp = [&](int sa, int sb, int h) {
-        const uint64_t ba = ring_k + sa * tile16 + h * half16;
-        const uint64_t bb = ring_k + sb * tile16 + h * half16;
+        const uint32_t row16 = kFull ? 0u : h * half16;
+        const uint32_t col = kFull ? 0u : h * G::HN;
+        const uint64_t ba = ring_k + sa * tile16 + row16;
+        const uint64_t bb = ring_k + sb * tile16 + row16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int p = (kk * 16) / G::PANEL_ELEMS;
             const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
             const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
             if constexpr (MODE == kBwdDQ)
-                mma_ts(tmem + G::T_S + h * G::HN, tmem + G::T_Q + kk * 8, ba + o16, idesc_half,
+                mma_ts(tmem + G::T_S + col, tmem + G::T_Q + kk * 8, ba + o16, idesc_half,
                        kk > 0 ? 1u : 0u);
             else
-                mma_ss(tmem + G::T_S + h * G::HN, fix_k + o16, ba + o16, idesc_half, kk > 0 ? 1u : 0u);
+                mma_ss(tmem + G::T_S + col, fix_k + o16, ba + o16, idesc_half, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -288,13 +297,14 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
             const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
             const uint32_t o16 = (p * G::PANEL_BYTES + off) >> 4;
             if constexpr (MODE == kBwdDQ)
-                mma_ts(tmem + G::T_P + h * G::HN, tmem + G::T_DO + kk * 8, bb + o16, idesc_half,
+                mma_ts(tmem + G::T_P + col, tmem + G::T_DO + kk * 8, bb + o16, idesc_half,
                        kk > 0 ? 1u : 0u);
             else
-                mma_ss(tmem + G::T_P + h * G::HN, fix_k + tile16 + o16, bb + o16, idesc_half,
+                mma_ss(tmem + G::T_P + col, fix_k + tile16 + o16, bb + o16, idesc_half,
                        kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(G::BAR_SF + h));
+        if (kFull) mma_commit(bar(G::BAR_SF + 1));  // both halves are there
     };
     // acc (+)= A[TMEM: 128 rows x HN, 16-bit, packed in HN/2 columns] times
     // B[HN rows x d, MN-major], 16 rows of B per MMA
@@ -316,8 +326,9 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
     // Software pipeline over half steps. For half h of step j the issuer
     // waits for the warps' P / dS of (j, h), queues the accumulation of
     // (j, h) and then S / dP of (j + 1, h) into the same columns (the tensor
-    // core runs in order, so the accumulation has read them first). The
-    // tensor core works on one half while the warps work on the other.
+    // core runs in order, so the accumulation has read them first; with
+    // whole-width S / dP, after the second half). The tensor core works on
+    // one half while the warps work on the other.
     int it_u = 0, base = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
@@ -351,7 +362,7 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
         }
         tc_fence_after();
         issue_sdp(sa, sb, 0);
-        issue_sdp(sa, sb, 1);
+        if (!kFull) issue_sdp(sa, sb, 1);
         for (int j = 0; ok && j < count; ++j) {
             const int gs = base + j;
             int na = 0, nb = 0;  // ring slots of step j + 1
@@ -384,15 +395,15 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
                     mma_commit(bar(G::BAR_RE + sa));
                     mma_commit(bar(G::BAR_RE + sb));
                 }
-                if (j + 1 < count) {
-                    if (h == 0) {
+                if (j + 1 < count && (!kFull || h == 1)) {
+                    if (h == 0 || kFull) {
                         if (!wait_ring(gs + 1, na, nb)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                     }
-                    issue_sdp(na, nb, h);
+                    issue_sdp(na, nb, kFull ? 0 : h);
                 }
             }
             if (!ok) break;

@@ -65,7 +65,7 @@ struct FwdGeom {
     static constexpr int SLOTS = D == 128 ? 5 : 8;
     // Q buffers (QT tiles each). Measured: one Q buffer and a deeper K/V ring
     // beat two Q buffers and a 3-slot ring at d = 128.
-    static constexpr int QBUF = 1;
+    static constexpr int QBUF = D <= 64 ? 2 : 1;  // next unit's Q loads early where smem allows
     static constexpr int Q_BUF_BYTES = QT * Q_TILE_BYTES;
     static constexpr uint32_t LAYOUT =
         ROW_BYTES == 128 ? kLayoutSw128 : (ROW_BYTES == 64 ? kLayoutSw64 : kLayoutSw32);

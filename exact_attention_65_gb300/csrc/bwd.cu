@@ -23,14 +23,16 @@
 //
 // Both are persistent kernels with the forward's roles: warp 0 is the TMA
 // producer (the unit's fixed pair of tiles, then a ring of streamed tiles),
-// one thread of warp 1 issues the tcgen05 MMAs, warps 4-7 hold one TMEM lane
-// (one row of the tile) per thread and do the elementwise work. For each
-// step the MMAs write the score tile and the dP tile to TMEM; the warps turn
-// them into 16-bit P and dS written back in place; then the accumulating
-// MMAs read them from TMEM.
+// one thread of warp 1 issues the tcgen05 MMAs, warps 4-11 hold one TMEM lane
+// (one row of the tile) per thread in two groups that split the columns, and
+// do the elementwise work. For each step the MMAs write the score tile and
+// the dP tile to TMEM; the warps turn them into 16-bit P and dS written back
+// in place, a 64-column half at a time; then the accumulating MMAs read them
+// from TMEM, the first half's while the warps work on the second.
 //
 // TMEM columns: [0, 128) score tile (then P or dS), [128, 256) dP tile (then
-// dS in the dK/dV kernel), [256, 256 + d) dQ or dV, [384, 384 + d) dK.
+// dS in the dK/dV kernel), [256, 256 + d) dQ or dV, [384, 384 + d) dK; the
+// dQ kernel keeps Q and dO as 16-bit MMA operands in [384, 384 + d).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,8 +44,11 @@ namespace {
 
 constexpr int kBwdDQ = 0;   // query-tile units: dQ
 constexpr int kBwdDKV = 1;  // key-tile units: dK and dV
-// warp 0 producer, warp 1 MMA issuer, warps 2-3 idle, warps 4-7 elementwise
-constexpr int kBwdThreads = 256;
+// warp 0 producer, warp 1 MMA issuer, warps 2-3 idle, warps 4-11 elementwise
+// (two groups of four: each group holds all 128 TMEM lanes, and group g takes
+// columns [32g, 32g + 32) of every 64-column half of the score tile)
+constexpr int kBwdThreads = 384;
+constexpr int kBwdComputeWarps = 8;
 
 template <int D>
 struct BwdGeom {
@@ -254,11 +259,10 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     // Width of the S / dP MMAs. A 128 x 64 MMA takes about as long on the
-    // tensor core as a 128 x 128 one, so the key-tile kernel (four products
-    // per step, tensor-bound) makes S and dP whole; the query-tile kernel
-    // makes them in halves, which lets the tensor core work on one half while
-    // the warps work on the other.
-    constexpr bool kFull = MODE == kBwdDKV;
+    // tensor core as a 128 x 128 one, so S and dP are made whole; the warps
+    // still hand P / dS over a half at a time, and the first half's
+    // accumulation runs while they work on the second.
+    constexpr bool kFull = true;
     constexpr uint32_t idesc_half = mma_idesc_f16(G::BT, kFull ? G::BT : G::HN, BF16, false, false);
     constexpr uint32_t idesc_acc = mma_idesc_f16(G::BT, D, BF16, false, true);      // 128 x d, B MN-major
     // K-major and MN-major descriptors of the fixed tiles and of ring slot 0
@@ -306,12 +310,14 @@ __device__ __forceinline__ void bwd_mma(uint32_t sbase, uint32_t tmem, int ntile
         mma_commit(bar(G::BAR_SF + h));
         if (kFull) mma_commit(bar(G::BAR_SF + 1));  // both halves are there
     };
-    // acc (+)= A[TMEM: 128 rows x HN, 16-bit, packed in HN/2 columns] times
-    // B[HN rows x d, MN-major], 16 rows of B per MMA
+    // acc (+)= A[TMEM: 128 rows x HN, 16-bit] times B[HN rows x d, MN-major],
+    // 16 rows of B per MMA. The warp group that made columns [32g, 32g + 32)
+    // of the half packed them into the half's columns [32g, 32g + 16).
     auto mma_acc_half = [&](uint32_t dst, uint32_t a_tmem, uint64_t bdesc_mn, bool first) {
 #pragma unroll
         for (int kk = 0; kk < G::HN / 16; ++kk)
-            mma_ts(dst, a_tmem + kk * 8, bdesc_mn + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_acc,
+            mma_ts(dst, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8,
+                   bdesc_mn + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_acc,
                    (!first || kk > 0) ? 1u : 0u);
     };
     // ring slots of global step gs, waited for until loaded
@@ -447,8 +453,8 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t *d
 }
 
 template <int D, int MODE, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint32_t tmem, int q4, int ntiles,
-                                            int nsteps, int units, const BwdArgs &a,
+__device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint32_t tmem, int q4, int cg,
+                                            int ntiles, int nsteps, int units, const BwdArgs &a,
                                             const WaitGuard &g) {
     using G = BwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
@@ -480,12 +486,15 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                 // row j*128 + row. Double-buffered by step parity; the buffer is
                 // rewritten two steps later, after every warp has passed the
                 // barrier of the step in between.
+                // (group 0 stages, both groups read)
                 float *buf = reinterpret_cast<float *>(smem + G::OFF_LD) + (step & 1) * 2 * G::BT;
-                const int qr = tj * G::BT + row;
-                buf[row] = qr < a.sq ? a.lse[bh * a.sq + qr] * kLog2e : INFINITY;
-                buf[G::BT + row] = qr < a.sq ? a.dvec[bh * a.sq + qr] : 0.f;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(G::BAR_LD + (step & 1)));
+                if (cg == 0) {
+                    const int qr = tj * G::BT + row;
+                    buf[row] = qr < a.sq ? a.lse[bh * a.sq + qr] * kLog2e : INFINITY;
+                    buf[G::BT + row] = qr < a.sq ? a.dvec[bh * a.sq + qr] : 0.f;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(G::BAR_LD + (step & 1)));
+                }
                 const bool okl = mbar_wait(bar(G::BAR_LD + (step & 1)), (step >> 1) & 1, g, 15);
                 if (!__all_sync(0xffffffffu, okl)) return;
                 ldbuf = buf;
@@ -501,8 +510,8 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                     // dS = P (dP - D); keys past sk (TMA zero fill) take no part.
                     // (causal: the row's own last visible key)
                     const int kv = (CAUSAL ? min(a.sk, grow + a.sk - a.sq + 1) : a.sk) - tj * G::BT - hc;
-#pragma unroll
-                    for (int c0 = 0; c0 < G::HN; c0 += 32) {
+                    {
+                        const int c0 = 32 * cg;  // this group's columns of the half
                         uint32_t sv[32], pv[32];
                         tmem_ld32(tmem + lanes + G::T_S + hc + c0, sv);
                         tmem_ld32(tmem + lanes + G::T_P + hc + c0, pv);
@@ -518,8 +527,9 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                             pk[i] = pack2b<BF16>(p0 * (__uint_as_float(pv[2 * i]) - drow),
                                                  p1 * (__uint_as_float(pv[2 * i + 1]) - drow));
                         }
-                        // dS of the half's keys c0 .. c0+31 into its columns c0/2 .. c0/2+15
-                        tmem_st16(tmem + lanes + G::T_S + hc + c0 / 2, pk);
+                        // dS of the half's keys c0 .. c0+31 into its columns c0 .. c0+15
+                        // (read already, by this thread)
+                        tmem_st16(tmem + lanes + G::T_S + hc + c0, pk);
                     }
                 } else {
                     // row = key row; columns = query rows tj*128 + hc .. with their
@@ -528,8 +538,8 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                     const float4 *ld4 = reinterpret_cast<const float4 *>(ldbuf);
                     // causal: this key row is seen by the tile's query columns >= cmin
                     const int cmin = CAUSAL ? grow - (a.sk - a.sq) - tj * G::BT : -1;
-#pragma unroll
-                    for (int c0 = 0; c0 < G::HN; c0 += 32) {
+                    {
+                        const int c0 = 32 * cg;  // this group's columns of the half
                         uint32_t sv[32], pv[32];
                         tmem_ld32(tmem + lanes + G::T_S + hc + c0, sv);
                         tmem_ld32(tmem + lanes + G::T_P + hc + c0, pv);
@@ -555,9 +565,9 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
                             pd[2 * q + 1] = pack2b<BF16>(dr[2], dr[3]);
                         }
                         // P^T and dS^T of the half's columns c0 .. c0+31 into its
-                        // columns c0/2 .. c0/2+15
-                        tmem_st16(tmem + lanes + G::T_S + hc + c0 / 2, pp);
-                        tmem_st16(tmem + lanes + G::T_P + hc + c0 / 2, pd);
+                        // columns c0 .. c0+15 (read already, by this thread)
+                        tmem_st16(tmem + lanes + G::T_S + hc + c0, pp);
+                        tmem_st16(tmem + lanes + G::T_P + hc + c0, pd);
                     }
                 }
                 tmem_wait_st();
@@ -572,19 +582,25 @@ __device__ __forceinline__ void bwd_compute(uint8_t *smem, uint32_t sbase, uint3
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
         const float scale = a.scale;
+        // each group stores half of the columns (d = 16: group 0 all of them)
+        constexpr int EC = D >= 32 ? D / 2 : D;
+        const int e0 = D >= 32 ? cg * EC : 0;
+        const bool mine = D >= 32 || cg == 0;
         if constexpr (MODE == kBwdDQ) {
             const bool out = grow < a.sq;
             uint16_t *dst = reinterpret_cast<uint16_t *>(a.dq) +
                             ((static_cast<int64_t>(x.batch) * a.sq + (out ? grow : 0)) * a.h + x.head) * D;
-            store_row<D, BF16>(tmem + lanes + G::T_A0, scale, dst, out, count == 0);
+            if (mine) store_row<EC, BF16>(tmem + lanes + G::T_A0 + e0, scale, dst + e0, out, count == 0);
         } else {
             const bool out = grow < a.sk;
             const int64_t off =
-                ((static_cast<int64_t>(x.batch) * a.sk + (out ? grow : 0)) * a.h + x.head) * D;
-            store_row<D, BF16>(tmem + lanes + G::T_A0, 1.0f, reinterpret_cast<uint16_t *>(a.dv) + off, out,
-                               count == 0);
-            store_row<D, BF16>(tmem + lanes + G::T_A1, scale, reinterpret_cast<uint16_t *>(a.dk) + off,
-                               out, count == 0);
+                ((static_cast<int64_t>(x.batch) * a.sk + (out ? grow : 0)) * a.h + x.head) * D + e0;
+            if (mine) {
+                store_row<EC, BF16>(tmem + lanes + G::T_A0 + e0, 1.0f,
+                                    reinterpret_cast<uint16_t *>(a.dv) + off, out, count == 0);
+                store_row<EC, BF16>(tmem + lanes + G::T_A1 + e0, scale,
+                                    reinterpret_cast<uint16_t *>(a.dk) + off, out, count == 0);
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -616,10 +632,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_MISC + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i)
-            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_PF + 1 || i == G::BAR_AE ||
-                               i == G::BAR_LD || i == G::BAR_LD + 1)
-                                  ? 4u    // one per compute warp
-                                  : 1u);
+            mbar_init(bar(i), (i == G::BAR_PF || i == G::BAR_PF + 1 || i == G::BAR_AE)
+                                  ? static_cast<uint32_t>(kBwdComputeWarps)  // one per compute warp
+                                  : (i == G::BAR_LD || i == G::BAR_LD + 1) ? 4u  // the staging group
+                                                                           : 1u);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -643,8 +659,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) bwd_mma<D, MODE, BF16, CAUSAL>(sbase, tmem, ntiles, nsteps, units, a, g);
-    } else if (warp >= 4 && warp < 8) {
-        bwd_compute<D, MODE, BF16, CAUSAL>(smem, sbase, tmem, warp & 3, ntiles, nsteps, units, a, g);
+    } else if (warp >= 4 && warp < 4 + kBwdComputeWarps) {
+        bwd_compute<D, MODE, BF16, CAUSAL>(smem, sbase, tmem, warp & 3, (warp - 4) >> 2, ntiles,
+                                           nsteps, units, a, g);
     }
 
     tc_fence_before();

@@ -82,15 +82,17 @@ struct DeviceState {
     int num_sms = 0;
     // copy streams of the host-buffer forward, made on first use
     cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
-    // arrival counters of the split decode's in-kernel reduce, one array per
-    // stream (calls on one stream are ordered, so its counters are all zero
-    // whenever a call starts)
-    struct Arrivals {
+    // The split decode's workspace, one per stream: arrival counters of the
+    // in-kernel reduce (all zero whenever a call starts) and the per-split
+    // partials. Calls on one stream are ordered, so each call may reuse them.
+    struct StreamWs {
         cudaStream_t stream;
-        uint32_t *p;
-        int64_t n;
+        uint32_t *counters;
+        int64_t n_counters;
+        void *part;
+        size_t part_bytes;
     };
-    std::vector<Arrivals> arrivals;
+    std::vector<StreamWs> stream_ws;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -143,40 +145,58 @@ attn_status_t copy_streams(DeviceState *ds) {
     return ATTN_OK;
 }
 
-// At least n zeroed arrival counters for `stream` (grown stream-ordered,
-// on that stream). nullptr, and the combine kernel, while the stream is being
-// captured into a graph: replays of a graph could run concurrently.
-uint32_t *arrival_counters(DeviceState *ds, cudaStream_t stream, int64_t n) {
+// The split decode's per-stream workspace: at least n zeroed arrival
+// counters and part_bytes of partials, grown stream-ordered on `stream`
+// (what is replaced is freed after the work already queued there). False
+// while the stream is being captured into a graph, whose replays could run
+// concurrently: the caller then takes a workspace per call and the separate
+// reduce kernel.
+bool stream_workspace(DeviceState *ds, cudaStream_t stream, int64_t n, size_t part_bytes,
+                      uint32_t **counters, void **part) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
         cudaGetLastError();
-        return nullptr;
+        return false;
     }
-    if (cs != cudaStreamCaptureStatusNone) return nullptr;
+    if (cs != cudaStreamCaptureStatusNone) return false;
     std::lock_guard<std::mutex> lock(g_mu);
-    DeviceState::Arrivals *e = nullptr;
-    for (auto &x : ds->arrivals)
+    DeviceState::StreamWs *e = nullptr;
+    for (auto &x : ds->stream_ws)
         if (x.stream == stream) e = &x;
-    if (e != nullptr && e->n >= n) return e->p;
-    const int64_t cap = n < 1024 ? 1024 : n;
-    uint32_t *p = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&p), cap * sizeof(uint32_t), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
+    if (e == nullptr) {
+        ds->stream_ws.push_back(DeviceState::StreamWs{stream, nullptr, 0, nullptr, 0});
+        e = &ds->stream_ws.back();
     }
-    if (cudaMemsetAsync(p, 0, cap * sizeof(uint32_t), stream) != cudaSuccess) {
-        cudaFreeAsync(p, stream);
-        cudaGetLastError();
-        return nullptr;
+    if (e->n_counters < n) {
+        const int64_t cap = n < 1024 ? 1024 : n;
+        uint32_t *p = nullptr;
+        if (cudaMallocAsync(reinterpret_cast<void **>(&p), cap * sizeof(uint32_t), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        if (cudaMemsetAsync(p, 0, cap * sizeof(uint32_t), stream) != cudaSuccess) {
+            cudaFreeAsync(p, stream);
+            cudaGetLastError();
+            return false;
+        }
+        if (e->counters != nullptr) cudaFreeAsync(e->counters, stream);
+        e->counters = p;
+        e->n_counters = cap;
     }
-    if (e != nullptr) {
-        cudaFreeAsync(e->p, stream);  // after the work already queued on it
-        e->p = p;
-        e->n = cap;
-    } else {
-        ds->arrivals.push_back(DeviceState::Arrivals{stream, p, cap});
+    if (e->part_bytes < part_bytes) {
+        const size_t cap = part_bytes < (1u << 20) ? (1u << 20) : part_bytes;
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, cap, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        if (e->part != nullptr) cudaFreeAsync(e->part, stream);
+        e->part = p;
+        e->part_bytes = cap;
     }
-    return p;
+    *counters = e->counters;
+    *part = e->part;
+    return true;
 }
 
 CUtensorMapSwizzle fwd_swizzle(int d) {
@@ -203,6 +223,35 @@ attn_status_t alloc_partials(int64_t splits, int b, int sq, int h, int d, cudaSt
     *o_part = static_cast<float *>(*ws);
     *lse_part = reinterpret_cast<float *>(static_cast<char *>(*ws) + o_bytes);
     return ATTN_OK;
+}
+
+// The CUDA-core split decode with splits > 1 (a.o, a.lse, sizes and splits
+// set): the stream's own workspace and the in-kernel reduce, or, while the
+// stream is being captured, a workspace of its own and the reduce kernel.
+attn_status_t run_split_decode(DeviceState *ds, int d, bool bf16, const CUtensorMap &tk,
+                               const CUtensorMap &tv, DecodeArgs &a, cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(a.b) * a.sq * a.h;
+    const size_t o_bytes = static_cast<size_t>(a.splits * rows * d) * sizeof(float);
+    const size_t l_bytes = static_cast<size_t>(a.splits * rows) * sizeof(float);
+    uint32_t *counters = nullptr;
+    void *part = nullptr;
+    if (stream_workspace(ds, stream, static_cast<int64_t>(a.b) * cdiv(a.sq, dec_rows_per_cta(a.sq)) * a.h,
+                         o_bytes + l_bytes, &counters, &part)) {
+        a.arrivals = counters;
+        a.o_part = static_cast<float *>(part);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(part) + o_bytes);
+        return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+    void *ws = nullptr;
+    attn_status_t st = alloc_partials(a.splits, a.b, a.sq, a.h, d, stream, &ws, &a.o_part, &a.lse_part);
+    if (st != ATTN_OK) return st;
+    a.arrivals = nullptr;
+    cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
+    if (e == cudaSuccess)
+        e = launch_combine(d, bf16, a.o_part, a.lse_part, static_cast<void *>(a.o), a.lse, a.b, a.sq, a.h,
+                           a.splits, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // The tensor-core forward kernel, over all keys (splits = 1) or over key
@@ -584,15 +633,7 @@ attn_status_t attn_decode_splitkv_ex(const void *q, const void *k, const void *v
     if (splits == 1)
         return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 
-    void *ws = nullptr;
-    if ((st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
-        return st;
-    a.arrivals = arrival_counters(ds, stream, static_cast<int64_t>(b) * cdiv(sq, dec_rows_per_cta(sq)) * h);
-    cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
-    if (e == cudaSuccess && a.arrivals == nullptr)
-        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+    return run_split_decode(ds, d, bf16, tk, tv, a, stream);
 }
 
 attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const void *v, void *o,
@@ -674,15 +715,7 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     a.num_pages = num_pages;
     if (splits == 1)
         return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-    void *ws = nullptr;
-    if ((st = alloc_partials(splits, b, 1, h, d, stream, &ws, &a.o_part, &a.lse_part)) != ATTN_OK)
-        return st;
-    a.arrivals = arrival_counters(ds, stream, static_cast<int64_t>(b) * h);
-    cudaError_t e = launch_decode(d, bf16, tk, tv, a, stream);
-    if (e == cudaSuccess && a.arrivals == nullptr)
-        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, 1, h, a.splits, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+    return run_split_decode(ds, d, bf16, tk, tv, a, stream);
 }
 
 attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -713,8 +746,11 @@ void attn_release_workspace(void) {
     cudaDeviceSynchronize();
     if (dev < kMaxDevices) {
         std::lock_guard<std::mutex> lock(g_mu);
-        for (auto &x : g_dev[dev].arrivals) cudaFree(x.p);
-        g_dev[dev].arrivals.clear();
+        for (auto &x : g_dev[dev].stream_ws) {
+            if (x.counters) cudaFree(x.counters);
+            if (x.part) cudaFree(x.part);
+        }
+        g_dev[dev].stream_ws.clear();
     }
     cudaMemPool_t pool;
     if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) cudaMemPoolTrimTo(pool, 0);

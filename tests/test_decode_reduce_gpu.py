@@ -5,7 +5,8 @@ arrival counters), against the fp64 oracle.
 Cases: many calls in a row on one stream with changing split counts and
 shapes (the counters must come back to zero after every call), a shape
 with more (batch, head) pairs than the first counter array holds (it is
-grown), a second stream with its own counters, results bit-identical to
+grown), partials that outgrow the stream's workspace, a second stream with
+its own counters, results bit-identical to
 the separate reduce kernel, which a call captured into a CUDA graph uses
 (replayed twice), and the paged cache. Tolerance: |O| 2e-2, LSE 1e-3.
 """
@@ -109,3 +110,16 @@ def test_many_splits(gpu, oracle_mod, splits):
         o, lse = gpu.attn_decode_splitkv(q.cuda(), k.cuda(), v.cuda(), num_splits=splits)
         assert gpu.attn_get_device_status() == gpu.ATTN_OK
         compare(o, lse, *oracle_mod.attention(q, k, v, 1 / math.sqrt(128)))
+
+
+def test_stream_workspace_grows_and_is_reused(gpu, oracle_mod):
+    """Partials of 16 splits x 384 (batch, head) rows x d = 128 in fp32 (3 MB)
+    outgrow the stream's first workspace; smaller calls after it reuse the
+    grown one."""
+    big = _qkv(8, 4096, 48, seed=21)
+    small = _qkv(1, 3000, 4, seed=22)
+    refs = {id(x): oracle_mod.attention(*x, 1 / math.sqrt(128)) for x in (big, small)}
+    for x, splits in ((small, 5), (big, 16), (small, 7), (big, 9), (small, 3)):
+        o, lse = gpu.attn_decode_splitkv(*(t.cuda() for t in x), num_splits=splits)
+        assert gpu.attn_get_device_status() == gpu.ATTN_OK
+        compare(o, lse, *refs[id(x)])

@@ -394,33 +394,42 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
     const size_t row = static_cast<size_t>(h) * d * 2;  // bytes of one sequence position
     const size_t qbat = row * sq, kbat = row * sk, lbat = static_cast<size_t>(h) * sq * sizeof(float);
 
-    // The plan: whole batches per chunk; a single non-causal batch is cut
-    // into ranges of query rows (multiples of the kernel's 256-row block, so
-    // every row sees the same tiles as in one call) after K and V are in.
+    // The plan (at most 8 chunks): whole batches per chunk; one batch
+    // without the mask is cut into ranges of query rows (multiples of the
+    // kernel's 256-row block, so every row sees the same tiles as in one
+    // call), its K and V going up with the first range. (Cutting several
+    // batches into row ranges as well made b4 s512 slower: 2 MB copies and
+    // twice the events and launches cost more than the shorter tail gains.)
     HostChunk plan[kHostChunks];
     int n = 0;
     bool by_rows = false;
-    if (b >= 2) {
+    const int blk = FWD_BM * FWD_QTILES;
+    int ranges = 1;  // row ranges per batch
+    if (!causal && b == 1 && sq >= 2 * blk)
+        ranges = static_cast<int>(cdiv(sq, blk) < kHostRowChunks ? cdiv(sq, blk) : kHostRowChunks);
+    if (ranges > 1) {
+        const int per = static_cast<int>(cdiv(cdiv(sq, ranges), blk) * blk);
+        for (int bb = 0; bb < b; ++bb)
+            for (int r0 = 0; r0 < sq; r0 += per)
+                plan[n++] = HostChunk{bb, 1, r0, sq - r0 < per ? sq - r0 : per};
+        by_rows = true;
+    } else if (b >= 2) {
         const int nc = b < kHostChunks ? b : kHostChunks;
         for (int i = 0; i < nc; ++i) {
             const int b0 = static_cast<int>(static_cast<int64_t>(b) * i / nc);
             const int b1 = static_cast<int>(static_cast<int64_t>(b) * (i + 1) / nc);
             plan[n++] = HostChunk{b0, b1 - b0, 0, sq};
         }
-    } else if (!causal && sq >= 2 * FWD_BM * FWD_QTILES) {
-        const int blk = FWD_BM * FWD_QTILES;
-        const int per = static_cast<int>(cdiv(cdiv(sq, kHostRowChunks), blk) * blk);
-        for (int r0 = 0; r0 < sq; r0 += per) plan[n++] = HostChunk{0, 1, r0, sq - r0 < per ? sq - r0 : per};
-        by_rows = n > 1;
     } else {
         plan[n++] = HostChunk{0, b, 0, sq};
     }
 
-    // Device workspace Q, K, V, O, LSE (+ per-row-chunk LSE [h, rows]), one
-    // stream-ordered allocation on `stream`.
+    // Device workspace Q, K, V, O, LSE (+ with row ranges, LSE [h, rows] of
+    // each chunk at [batch, h * row0]), one stream-ordered allocation on
+    // `stream`.
     const size_t oq = 0, ok_ = round_up(oq + qbat * b, 256), ov = round_up(ok_ + kbat * b, 256),
                  oo = round_up(ov + kbat * b, 256), ol = round_up(oo + qbat * b, 256),
-                 ot = round_up(ol + lbat * b, 256), total = ot + (by_rows ? lbat : 0);
+                 ot = round_up(ol + lbat * b, 256), total = ot + (by_rows ? lbat * b : 0);
     char *ws = nullptr;
     if (cudaMallocAsync(reinterpret_cast<void **>(&ws), total, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -444,8 +453,8 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
     if (good) good = cudaStreamWaitEvent(ds->s_d2h, ev_start, 0) == cudaSuccess;
     for (int c = 0; c < n && good; ++c) {
         const HostChunk &x = plan[c];
-        // in: K and V of the chunk's batches (once, when cut by rows), then its Q rows
-        if (!by_rows || c == 0) {
+        // in: K and V of the chunk's batches (with its first row range), then its Q rows
+        if (x.r0 == 0) {
             h2d(ok_ + kbat * x.b0, hk + kbat * x.b0, kbat * x.nb);
             h2d(ov + kbat * x.b0, hv + kbat * x.b0, kbat * x.nb);
         }
@@ -454,7 +463,8 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
         if (good) good = cudaEventRecord(ev[2 * c], ds->s_h2d) == cudaSuccess;
         // compute on the caller's stream
         if (good) good = cudaStreamWaitEvent(stream, ev[2 * c], 0) == cudaSuccess;
-        float *lse_dev = by_rows ? reinterpret_cast<float *>(ws + ot) + static_cast<size_t>(h) * x.r0
+        float *lse_dev = by_rows ? reinterpret_cast<float *>(ws + ot) + static_cast<size_t>(h) * sq * x.b0 +
+                                       static_cast<size_t>(h) * x.r0
                                  : reinterpret_cast<float *>(ws + ol) + static_cast<size_t>(h) * sq * x.b0;
         if (good)
             good = run_fwd(ws + oq + qoff, ws + ok_ + kbat * x.b0, ws + ov + kbat * x.b0, ws + oo + qoff,
@@ -467,8 +477,9 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
             good = cudaMemcpyAsync(ho + qoff, ws + oo + qoff, qbytes, cudaMemcpyDeviceToHost,
                                    ds->s_d2h) == cudaSuccess;
         if (good) {
-            if (by_rows)  // LSE [h, rows] into the rows' columns of [h, sq]
-                good = cudaMemcpy2DAsync(lse + x.r0, static_cast<size_t>(sq) * sizeof(float), lse_dev,
+            if (by_rows)  // LSE [h, rows] into the rows' columns of the batch's [h, sq]
+                good = cudaMemcpy2DAsync(lse + static_cast<size_t>(h) * sq * x.b0 + x.r0,
+                                         static_cast<size_t>(sq) * sizeof(float), lse_dev,
                                          static_cast<size_t>(x.nr) * sizeof(float),
                                          static_cast<size_t>(x.nr) * sizeof(float), h,
                                          cudaMemcpyDeviceToHost, ds->s_d2h) == cudaSuccess;

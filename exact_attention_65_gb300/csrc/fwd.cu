@@ -167,7 +167,9 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
                                              const WaitGuard &g) {
     using G = FwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
-    const uint64_t keep = policy_evict_last();  // K/V are re-read by every query block of the head
+    // K/V are re-read by every query block of the head; with one query block
+    // they are read once, and kept out of the way in L2 instead
+    const uint64_t keep = nqb > 1 ? policy_evict_last() : policy_evict_first();
 
     int q_issued = 0, n_issued = 0;  // n counts ring items (K and V tiles)
     bool ok = true;

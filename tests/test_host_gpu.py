@@ -5,7 +5,7 @@ oracle within the forward's tolerance (|O| 2e-2, LSE 1e-3).
 
 Chunkings covered: several batches (one and more per chunk, more batches
 than chunks), one non-causal batch cut into query-row ranges (ragged last
-range, LSE gathered back into [h, sq]), one causal batch (single chunk),
+range, LSE gathered back into [h, sq]), causal batches (whole batches),
 pinned and pageable host memory, fp16 and bf16, and the call queued
 without synchronising (sync=False) and read after the stream is done.
 """
@@ -47,7 +47,9 @@ def _check(ea, oracle_mod, b, sq, sk, h, d, dtype, causal=False, pin=True, seed=
 
 
 @pytest.mark.parametrize("b,sq,sk,h,d", [(4, 300, 200, 2, 128), (2, 64, 1000, 3, 64),
-                                         (11, 130, 77, 2, 32), (3, 1, 513, 2, 128)])
+                                         (11, 130, 77, 2, 32), (3, 1, 513, 2, 128),
+                                         (4, 512, 512, 3, 128), (3, 1000, 333, 2, 64),
+                                         (9, 600, 100, 2, 32)])
 def test_host_batches(gpu, oracle_mod, b, sq, sk, h, d):
     _check(gpu, oracle_mod, b, sq, sk, h, d, torch.bfloat16)
 

@@ -37,7 +37,10 @@
 namespace exattn {
 namespace {
 
-template <int D>
+// ST stages of K/V blocks in flight. One split per (batch, head) streams a
+// long range per CTA and gains from a fourth stage (b8 h48 sk8192: 277 ->
+// 256 us); split launches, whose CTAs all start at once, lose from it.
+template <int D, int ST>
 struct DecGeom {
     static constexpr int LPR = D / 8;           // lanes per key row
     static constexpr int RPP = 32 / LPR;        // rows per warp pass
@@ -49,7 +52,7 @@ struct DecGeom {
     static constexpr int ROWS_PER_WARP = BN / NCW;
     static constexpr int PASSES = ROWS_PER_WARP / RPP;
     static constexpr int GROUPS = NCW * RPP;    // independent softmax states per query
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = ST;
     static constexpr int BLOCK_BYTES = BN * D * 2;
     static constexpr int STAGE_BYTES = 2 * BLOCK_BYTES;  // K block then V block
     static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
@@ -107,12 +110,12 @@ __device__ __forceinline__ bool consumer_sync_any(bool pred, int nthreads) {
     return r != 0;
 }
 
-template <int D, int QR, bool BF16, bool PAGED, typename Full, typename Empty>
+template <int D, int ST, int QR, bool BF16, bool PAGED, typename Full, typename Empty>
 __device__ __forceinline__ void decode_consume(uint8_t *smem, Full full, Empty empty, int warp,
                                                int lane, int split, int head, int batch, int q0,
                                                int nq, int blk0, int blk1, int row_end,
                                                const DecodeArgs &a, const WaitGuard &g) {
-    using G = DecGeom<D>;
+    using G = DecGeom<D, ST>;
     volatile uint32_t *abort_flag = g.abort;
     const int grp = lane / G::LPR;  // row slot within a pass
     const int sub = lane % G::LPR;  // which 8 elements of the row
@@ -400,11 +403,11 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
     if (lane == 0) lse[lse_idx] = L;
 }
 
-template <int D, int QR, bool BF16, bool PAGED>
-__global__ void __launch_bounds__(DecGeom<D>::THREADS)
+template <int D, int ST, int QR, bool BF16, bool PAGED>
+__global__ void __launch_bounds__(DecGeom<D, ST>::THREADS)
     decode_split_kernel(const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const DecodeArgs a) {
-    using G = DecGeom<D>;
+    using G = DecGeom<D, ST>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 127u) & ~127u;
@@ -478,8 +481,8 @@ __global__ void __launch_bounds__(DecGeom<D>::THREADS)
                 mbar_wait(full(i % G::STAGES), (i / G::STAGES) & 1, drain, 2);
         }
     } else {
-        decode_consume<D, QR, BF16, PAGED>(smem, full, empty, warp, lane, split, head, batch, q0, nq, blk0,
-                                    blk1, row_end, a, g);
+        decode_consume<D, ST, QR, BF16, PAGED>(smem, full, empty, warp, lane, split, head, batch, q0,
+                                               nq, blk0, blk1, row_end, a, g);
     }
     __syncthreads();
 
@@ -526,32 +529,37 @@ __global__ void __launch_bounds__(128)
     combine_row<D, BF16>(o_part, lse_part, o, lse, b, sq, h, splits, batch, qrow, head, lane);
 }
 
-template <int D, int QR, bool BF16, bool PAGED>
+template <int D, int ST, int QR, bool BF16, bool PAGED>
 cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                             cudaStream_t stream) {
-    using G = DecGeom<D>;
+    using G = DecGeom<D, ST>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<D, QR, BF16, PAGED>,
+        e = cudaFuncSetAttribute(decode_split_kernel<D, ST, QR, BF16, PAGED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const int nqb = (a.sq + QR - 1) / QR;
     dim3 grid(a.splits, a.h, a.b * nqb);
-    decode_split_kernel<D, QR, BF16, PAGED><<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(tk, tv, a);
+    decode_split_kernel<D, ST, QR, BF16, PAGED><<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
 template <int D, bool BF16>
 cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                             cudaStream_t stream) {
-    if (a.block_table) return launch_decode_t<D, 1, BF16, true>(tk, tv, a, stream);  // sq == 1
-    if (a.sq == 1) return launch_decode_t<D, 1, BF16, false>(tk, tv, a, stream);
-    return launch_decode_t<D, 4, BF16, false>(tk, tv, a, stream);
+    const bool deep = a.splits == 1;
+    if (a.block_table)  // sq == 1
+        return deep ? launch_decode_t<D, 4, 1, BF16, true>(tk, tv, a, stream)
+                    : launch_decode_t<D, 3, 1, BF16, true>(tk, tv, a, stream);
+    if (a.sq == 1)
+        return deep ? launch_decode_t<D, 4, 1, BF16, false>(tk, tv, a, stream)
+                    : launch_decode_t<D, 3, 1, BF16, false>(tk, tv, a, stream);
+    return launch_decode_t<D, 3, 4, BF16, false>(tk, tv, a, stream);
 }
 
 template <int D, bool BF16>

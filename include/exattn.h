@@ -9,9 +9,10 @@
  *            innermost (the (b, s, h, d) layout "Why FlashAttention is
  *            fast" section 2 item 2 says flash_attn_func consumes directly,
  *            so no transposes are needed). lse: [b, h, sq], fp32.
- *   Memory   q, k, v, o, lse are DEVICE pointers on the current CUDA device,
- *            owned by the caller; the library never frees or keeps them.
- *            q, k, v, o must be 16-byte aligned, lse 4-byte aligned.
+ *   Memory   q, k, v, o, lse are DEVICE pointers on the current CUDA device
+ *            (attn_fwd_host alone takes host pointers), owned by the caller;
+ *            the library never frees or keeps them. q, k, v, o must be
+ *            16-byte aligned, lse 4-byte aligned.
  *   Streams  every compute call is asynchronous on `stream` (0 = legacy
  *            default stream). Argument errors are returned before anything
  *            is enqueued. A wait inside a kernel that exceeds its bound
@@ -44,7 +45,7 @@ typedef enum {
     ATTN_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, size < 1, non-finite scale, bad dtype */
     ATTN_ERR_UNSUPPORTED = 2,    /* d outside {16, 32, 64, 128}, or a size beyond the grid limits */
     ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed (launch, tensor-map encode, ...) */
-    ATTN_ERR_NO_MEMORY = 4,      /* the decode workspace could not be allocated */
+    ATTN_ERR_NO_MEMORY = 4,      /* a workspace (decode partials, backward, host forward) could not be allocated */
     ATTN_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up on a bounded wait (see attn_get_device_status) */
 } attn_status_t;
 
@@ -267,7 +268,12 @@ unsigned int attn_last_timeout_site(void);
 /* Static, human-readable name of a status code. */
 const char *attn_status_string(attn_status_t status);
 
-/* Returns cached decode workspace memory of the current device to the system. */
+/*
+ * Waits for the current device to finish its work, frees the split
+ * decode's per-stream workspaces (counters and partials; the next split
+ * decode on a stream makes them again) and returns the memory the device's
+ * default pool keeps cached to the system.
+ */
 void attn_release_workspace(void);
 
 /*

@@ -123,3 +123,16 @@ def test_stream_workspace_grows_and_is_reused(gpu, oracle_mod):
         o, lse = gpu.attn_decode_splitkv(*(t.cuda() for t in x), num_splits=splits)
         assert gpu.attn_get_device_status() == gpu.ATTN_OK
         compare(o, lse, *refs[id(x)])
+
+
+def test_release_then_decode_again(gpu, oracle_mod):
+    """attn_release_workspace frees the per-stream counters and partials; the
+    next split decode on the same stream makes them again."""
+    q, k, v = _qkv(1, 5000, 4, seed=23)
+    ref = oracle_mod.attention(q, k, v, 1 / math.sqrt(128))
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    for _ in range(2):
+        o, lse = gpu.attn_decode_splitkv(qd, kd, vd, num_splits=6)
+        assert gpu.attn_get_device_status() == gpu.ATTN_OK
+        compare(o, lse, *ref)
+        gpu.attn_release_workspace()

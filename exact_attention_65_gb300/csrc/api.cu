@@ -387,6 +387,14 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
                             int causal, cudaStream_t stream) {
     attn_status_t st = validate_args(q, k, v, o, lse, b, sq, sk, h, d, scale, dtype);
     if (st != ATTN_OK) return st;
+    // The pipeline runs on the library's copy streams, joined to `stream` by
+    // events: not something to record into a graph.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return ATTN_ERR_UNSUPPORTED;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     if ((st = copy_streams(ds)) != ATTN_OK) return st;

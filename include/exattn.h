@@ -92,7 +92,8 @@ attn_status_t attn_fwd_causal(const void *q, const void *k, const void *v, void 
  * afterwards starts once every copy-back is done, so o and lse may be read
  * after `stream` is synchronised (the host buffers must stay valid until
  * then). Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be
- * had.
+ * had; ATTN_ERR_UNSUPPORTED while `stream` is being captured into a graph
+ * (the pipeline runs on the library's own copy streams).
  */
 attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
                             int b, int sq, int sk, int h, int d, float scale, attn_dtype_t dtype,
@@ -272,7 +273,8 @@ const char *attn_status_string(attn_status_t status);
  * Waits for the current device to finish its work, frees the split
  * decode's per-stream workspaces (counters and partials; the next split
  * decode on a stream makes them again) and returns the memory the device's
- * default pool keeps cached to the system.
+ * default pool keeps cached to the system. No other call of this library
+ * may run on the device meanwhile (from another host thread).
  */
 void attn_release_workspace(void);
 

@@ -76,3 +76,23 @@ def test_host_rejects_device_tensors(gpu):
     q = torch.zeros((1, 8, 1, 16), dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
         gpu.attn_fwd_host(q, q, q)
+
+
+def test_host_refuses_graph_capture(gpu):
+    """The pipeline uses the library's own copy streams: a captured call is
+    refused (ATTN_ERR_UNSUPPORTED) and the capture itself stays intact."""
+    q = torch.zeros((1, 8, 1, 16), dtype=torch.float16).pin_memory()
+    o = torch.empty_like(q).pin_memory()
+    lse = torch.empty((1, 1, 8), dtype=torch.float32).pin_memory()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    x = torch.zeros(4, device="cuda")
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            x.add_(1)
+            with pytest.raises(gpu.AttnError) as err:
+                gpu.attn_fwd_host(q, q, q, out=o, lse=lse, sync=False)
+            assert err.value.status == gpu.ATTN_ERR_UNSUPPORTED
+    graph.replay()
+    torch.cuda.synchronize()
+    assert x.tolist() == [1.0] * 4

@@ -292,6 +292,7 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     a.o_part = nullptr;
     a.lse_part = nullptr;
     a.causal = causal ? 1 : 0;
+    a.longest_first = causal ? 1 : 0;
     if (splits == 1)
         return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     void *ws = nullptr;

@@ -41,6 +41,9 @@ struct FwdArgs {
     // Causal mask, bottom-right aligned: query row i sees key j only if
     // j <= i + sk - sq; rows that see no key get O = 0 and LSE = -inf.
     int causal;
+    // Causal units in longest-first order across all (batch, head) pairs,
+    // instead of alternating the query-block order per (batch, head).
+    int longest_first;
 };
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -75,6 +75,11 @@ def load_library() -> ctypes.CDLL:
         for fn in (lib.attn_bwd, lib.attn_bwd_causal):
             fn.restype = i32
             fn.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_decode_splitkv_noalloc.restype = i32
+        lib.attn_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                    f32, i32, i32, vp]
+        lib.attn_get_noalloc_status.restype = i32
+        lib.attn_get_noalloc_status.argtypes = [vp]
         lib.attn_decode_num_splits.restype = i32
         lib.attn_decode_num_splits.argtypes = [i32] * 5
         lib.attn_decode_num_splits_for_sms.restype = i32
@@ -99,15 +104,22 @@ def attn_status_string(status: int) -> str:
     return load_library().attn_status_string(int(status)).decode()
 
 
+_DTYPE_CODE = {torch.float16: ATTN_FP16, torch.bfloat16: ATTN_BF16}
+_current_raw_stream = torch._C._cuda_getCurrentRawStream
+_current_device = torch._C._cuda_getDevice
+
+
 def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype == torch.float16:
-        return ATTN_FP16
-    if t.dtype == torch.bfloat16:
-        return ATTN_BF16
-    raise TypeError(f"exattn takes float16 or bfloat16 tensors, got {t.dtype}")
+    code = _DTYPE_CODE.get(t.dtype)
+    if code is None:
+        raise TypeError(f"exattn takes float16 or bfloat16 tensors, got {t.dtype}")
+    return code
 
 
 def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    """Sizes (b, sq, sk, h, d) and dtype code of a q, k, v triple; raises on
+    anything the C ABI would not take. Kept lean: small problems issue in a
+    few microseconds, and this runs on every call."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
@@ -115,14 +127,17 @@ def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
             raise ValueError(f"{name} must be [b, s, h, d], got shape {tuple(t.shape)}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous in (b, s, h, d) order")
-    if not (q.device == k.device == v.device):
-        raise ValueError("q, k, v must be on the same device")
-    if not (q.dtype == k.dtype == v.dtype):
+    dt = q.dtype
+    if k.dtype is not dt or v.dtype is not dt:
         raise TypeError("q, k, v must share one dtype")
+    dev = q.device
+    if k.device != dev or v.device != dev:
+        raise ValueError("q, k, v must be on the same device")
     b, sq, h, d = q.shape
-    if k.shape != v.shape or k.shape[0] != b or k.shape[2] != h or k.shape[3] != d:
+    kb, sk, kh, kd = k.shape
+    if kb != b or kh != h or kd != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
-    return b, sq, k.shape[1], h, d, _dtype_code(q)
+    return b, sq, sk, h, d, _dtype_code(q)
 
 
 def _outputs(q, out, lse, b, h, sq):
@@ -132,7 +147,7 @@ def _outputs(q, out, lse, b, h, sq):
         raise ValueError("out must be a contiguous tensor like q")
     if lse is None:
         lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
-    elif (tuple(lse.shape) != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
+    elif (lse.shape != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
           or lse.device != q.device):
         raise ValueError("lse must be a contiguous float32 tensor [b, h, sq]")
     return out, lse
@@ -142,6 +157,18 @@ def _stream(device, stream):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(fn, device, stream, *args):
+    """Call C-ABI function ``fn`` with ``args`` plus the stream, with
+    ``device`` current. The common case (device already current, its current
+    stream) skips the device context manager and the Stream object."""
+    idx = device.index
+    if idx == _current_device():
+        raw = _current_raw_stream(idx) if stream is None else stream.cuda_stream
+        return fn(*args, raw)
+    with torch.cuda.device(device):
+        return fn(*args, _stream(device, stream))
 
 
 def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=None,
@@ -155,11 +182,10 @@ def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=Non
     b, sq, sk, h, d, dt = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, b, h, sq)
-    lib = load_library()
+    lib = _lib or load_library()
     fn = lib.attn_fwd_causal if causal else lib.attn_fwd
-    with torch.cuda.device(q.device):
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+               lse.data_ptr(), b, sq, sk, h, d, scale, dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_causal" if causal else "attn_fwd")
     return out, lse
@@ -219,11 +245,10 @@ def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0
     b, sq, sk, h, d, dt = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, b, h, sq)
-    lib = load_library()
+    lib = _lib or load_library()
     fn = lib.attn_decode_splitkv_causal if causal else lib.attn_decode_splitkv_ex
-    with torch.cuda.device(q.device):
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                b, sq, sk, h, d, scale, int(num_splits), dt, _stream(q.device, stream))
+    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+               lse.data_ptr(), b, sq, sk, h, d, scale, int(num_splits), dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_splitkv")
     return out, lse
@@ -260,13 +285,11 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float 
     dt = _dtype_code(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, b, h, 1)
-    lib = load_library()
-    with torch.cuda.device(q.device):
-        rc = lib.attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
-                                   block_table.data_ptr(), seqlens_k.data_ptr(), out.data_ptr(),
-                                   lse.data_ptr(), b, h, d, num_pages, page_size,
-                                   block_table.shape[1], scale, int(num_splits), dt,
-                                   _stream(q.device, stream))
+    lib = _lib or load_library()
+    rc = _call(lib.attn_decode_paged, q.device, stream, q.data_ptr(), k_pages.data_ptr(),
+               v_pages.data_ptr(), block_table.data_ptr(), seqlens_k.data_ptr(), out.data_ptr(),
+               lse.data_ptr(), b, h, d, num_pages, page_size, block_table.shape[1], scale,
+               int(num_splits), dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged")
     return out, lse
@@ -294,15 +317,42 @@ def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None
     for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous() or t.device != q.device:
             raise ValueError(f"{name} must be a contiguous tensor like {name[1]}")
-    lib = load_library()
-    with torch.cuda.device(q.device):
-        fn = lib.attn_bwd_causal if causal else lib.attn_bwd
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                b, sq, sk, h, d, scale, dt, _stream(q.device, stream))
+    lib = _lib or load_library()
+    fn = lib.attn_bwd_causal if causal else lib.attn_bwd
+    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+               lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+               b, sq, sk, h, d, scale, dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd_causal" if causal else "attn_bwd")
     return dq, dk, dv
+
+
+def attn_decode_splitkv_noalloc(q, k, v, out, lse, scale: float | None = None,
+                                num_splits: int = 0, stream=None):
+    """attn_decode_splitkv for callers that cannot allocate device memory:
+    out and lse must be given, and the per-split partials live in a fixed
+    array inside the library (calls that overlap on the GPU race on it).
+    Its kernels' timeouts are read by attn_get_noalloc_status()."""
+    b, sq, sk, h, d, dt = _check(q, k, v)
+    if out is None or lse is None:
+        raise ValueError("out and lse must be given: this entry point allocates nothing")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, b, h, sq)
+    lib = _lib or load_library()
+    rc = _call(lib.attn_decode_splitkv_noalloc, q.device, stream, q.data_ptr(), k.data_ptr(),
+               v.data_ptr(), out.data_ptr(), lse.data_ptr(), b, sq, sk, h, d, scale,
+               int(num_splits), dt)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_splitkv_noalloc")
+    return out, lse
+
+
+def attn_get_noalloc_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the status word of the
+    no-allocation decode."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return load_library().attn_get_noalloc_status(_stream(device, stream))
 
 
 def attn_decode_num_splits(b: int, sq: int, sk: int, h: int, d: int) -> int:
@@ -336,7 +386,8 @@ def attn_debug_set_flags(flags: int) -> None:
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_host", "attn_bwd", "attn_decode_splitkv",
-    "attn_decode_paged", "attn_decode_num_splits",
+    "attn_decode_paged", "attn_decode_splitkv_noalloc", "attn_get_noalloc_status",
+    "attn_decode_num_splits",
     "attn_decode_num_splits_for_sms", "attn_get_device_status", "attn_last_timeout_site",
     "attn_release_workspace", "attn_debug_set_flags", "attn_status_string", "load_library",
 ]

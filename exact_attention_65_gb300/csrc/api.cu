@@ -99,6 +99,12 @@ DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 unsigned int g_last_site = 0;
 
+}  // namespace
+
+void exattn::record_timeout_site(unsigned int word) { g_last_site = word; }
+
+namespace {
+
 attn_status_t device_state(DeviceState **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
@@ -753,7 +759,7 @@ attn_status_t attn_get_device_status(cudaStream_t stream) {
     if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (word != 0) {
-        g_last_site = word;
+        record_timeout_site(word);
         if (cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;
         return ATTN_ERR_DEVICE_TIMEOUT;
     }

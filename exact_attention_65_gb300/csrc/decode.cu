@@ -556,10 +556,10 @@ cudaError_t launch_decode_d(const CUtensorMap &tk, const CUtensorMap &tv, const 
     if (a.block_table)  // sq == 1
         return deep ? launch_decode_t<D, 4, 1, BF16, true>(tk, tv, a, stream)
                     : launch_decode_t<D, 3, 1, BF16, true>(tk, tv, a, stream);
-    if (a.sq == 1)
-        return deep ? launch_decode_t<D, 4, 1, BF16, false>(tk, tv, a, stream)
-                    : launch_decode_t<D, 3, 1, BF16, false>(tk, tv, a, stream);
-    return launch_decode_t<D, 3, 4, BF16, false>(tk, tv, a, stream);
+    // Several query rows run on the tensor-core forward kernel instead.
+    if (a.sq != 1) return cudaErrorNotSupported;
+    return deep ? launch_decode_t<D, 4, 1, BF16, false>(tk, tv, a, stream)
+                : launch_decode_t<D, 3, 1, BF16, false>(tk, tv, a, stream);
 }
 
 template <int D, bool BF16>

@@ -75,7 +75,8 @@ constexpr int DEC_BLOCK_BYTES = 16384;
 constexpr int DEC_MAX_SPLITS = 1024;
 constexpr int dec_block_rows(int d) { return DEC_BLOCK_BYTES / (d * 2); }
 constexpr int dec_box_rows(int d) { return dec_block_rows(d) < 256 ? dec_block_rows(d) : 256; }
-// Query rows handled by one CTA.
+// Query rows handled by one CTA of the CUDA-core kernel (which runs sq == 1
+// only; several rows go to the tensor-core forward kernel).
 inline int dec_rows_per_cta(int sq) { return sq == 1 ? 1 : 4; }
 
 // Split count of the CUDA-core decode kernel for num_splits = 0: 1 when the
@@ -124,6 +125,8 @@ constexpr uint32_t kFlagSkipLoads = 1u;
 // None of these allocates device memory.
 bool load_tensor_map_encoder();
 unsigned int debug_flags();
+// Remembers a status word's (kernel, site) for attn_last_timeout_site().
+void record_timeout_site(unsigned int word);
 attn_status_t validate_args(const void *q, const void *k, const void *v, const void *o,
                             const float *lse, int b, int sq, int sk, int h, int d, float scale,
                             int dtype);

@@ -220,27 +220,40 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
  * process exits.
  *
  * Arguments, layouts and results are those of attn_decode_splitkv_ex; the
- * caller still passes all inputs and outputs. With more than one split the
- * partials need 4 * splits * b * sq * h * (d + 1) bytes (each part rounded
- * up to 256); a request that needs more than the array holds returns
- * ATTN_ERR_UNSUPPORTED before anything is enqueued.
+ * caller still passes all inputs and outputs. The kernels are the same:
+ * with sq == 1 the CUDA-core split kernel, with sq > 1 the tensor-core
+ * forward kernel split along the keys (tiles of 128 keys, a requested count
+ * lowered so that no split is empty), each followed by the combine kernel;
+ * num_splits = 0 picks the count attn_decode_num_splits() reports. With more
+ * than one split the partials need 4 * splits * b * sq * h * (d + 1) bytes
+ * (each part rounded up to 256); a request that needs more than the array
+ * holds returns ATTN_ERR_UNSUPPORTED before anything is enqueued.
  *
- * The first call on a device does a one-time set-up: it looks up the
- * array's device address and clears this entry point's status word with
- * cudaMemset (legacy default stream); make that first call before any
- * stream capture. All calls share the one
- * array, which keeps the last call's contents (every split rewrites all of
- * its partials, so none is read stale): calls that overlap on the GPU, from
- * different streams or host threads, race on it and must be serialised by
- * the caller. A bounded-wait timeout in this entry point's kernels is
- * recorded in its own status word and is not reported by
- * attn_get_device_status().
+ * The first call on a device does a one-time set-up (it looks up the
+ * array's device address; nothing is written); make that first call before
+ * any stream capture. All calls share the one array, which keeps the last
+ * call's contents (every split rewrites all of its partials, so none is
+ * read stale): calls that overlap on the GPU, from different streams or
+ * host threads, race on it and must be serialised by the caller. A
+ * bounded-wait timeout in this entry point's kernels is recorded in a
+ * status word of its own, read by attn_get_noalloc_status(), not by
+ * attn_get_device_status() (whose first use allocates its word).
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 attn_status_t attn_decode_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
                                           float *lse, int b, int sq, int sk, int h, int d,
                                           float scale, int num_splits, attn_dtype_t dtype,
                                           cudaStream_t stream);
+
+/*
+ * Status reader of attn_decode_splitkv_noalloc, allocating nothing either.
+ * Synchronises `stream`, then reports and clears that entry point's status
+ * word on the current device: ATTN_ERR_DEVICE_TIMEOUT if one of its kernels
+ * abandoned a bounded wait since the last call (attn_last_timeout_site()
+ * then names the kernel and wait), ATTN_ERR_CUDA if the stream reported an
+ * error, ATTN_OK otherwise (also before the entry point's first call).
+ */
+attn_status_t attn_get_noalloc_status(cudaStream_t stream);
 
 /*
  * The split heuristic for num_splits = 0 on the current device (same issue:

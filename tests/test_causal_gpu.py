@@ -69,18 +69,17 @@ def test_causal_decode_one_row_is_unmasked(gpu):
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
 
 
-def test_causal_mid_shape_sampled_rows(gpu, oracle_mod):
+def test_causal_mid_shape_all_rows(gpu, oracle_mod):
     w = workloads.WORKLOADS["mid_fwd"]
     q, k, v = workloads.make_workload(w)
     o, lse = gpu.attn_fwd(*(t.cuda() for t in (q, k, v)), causal=True)
-    rows = sorted(set([0, 1, 2, 127, 128, 129, 255, 256, 383, 384, 510, 511] +
-                      list(range(5, 512, 41))))
-    _check(gpu, oracle_mod, q, k, v, w.scale, o, lse, rows=rows)
+    _check(gpu, oracle_mod, q, k, v, w.scale, o, lse)
 
 
-def test_causal_long_strided_rows(gpu, oracle_mod):
-    b, s, h, d = 1, 4096, 8, 128
+def test_causal_several_units_per_cta_all_rows(gpu, oracle_mod):
+    """More causal units than SMs (b2 s1024 h48: 384 units dealt longest
+    first over 152 CTAs); every row is compared."""
+    b, s, h, d = 2, 1024, 48, 128
     q, k, v = _inputs(b, s, s, h, d, torch.bfloat16, 79)
     o, lse = gpu.attn_fwd(*(t.cuda() for t in (q, k, v)), causal=True)
-    rows = [r * 16 + (r % 16) for r in range(256)]
-    _check(gpu, oracle_mod, q, k, v, 1 / math.sqrt(d), o, lse, rows=rows)
+    _check(gpu, oracle_mod, q, k, v, 1 / math.sqrt(d), o, lse)

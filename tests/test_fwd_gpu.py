@@ -2,9 +2,10 @@
 
 Shapes: the tiny and small-head problems of the flash-attn timing issue
 (head dim 16, fp16), the b4 s512 h32 d128 bf16 problem of "Why
-FlashAttention is fast", the long b1 s8192 h32 d128 problem on 256 sampled
-rows, and edge cases: ragged query/key tails, fewer keys than one tile,
-single rows and keys, every head dim, both dtypes, zero and negative scale.
+FlashAttention is fast" on every row, a problem with more units than SMs on
+every row, the long b1 s8192 h32 d128 problem on 256 sampled rows, and edge
+cases: ragged query/key tails, fewer keys than one tile, single rows and
+keys, every head dim, both dtypes, zero and negative scale.
 Tolerance: max |O - O_ref| <= 2e-2 and max |LSE - LSE_ref| <= 1e-3.
 """
 import math
@@ -41,14 +42,26 @@ def test_pages_small_shapes_all_rows(gpu, oracle_mod, name):
     check_full(gpu, oracle_mod, w.b, w.sq, w.sk, w.h, w.d, w.dtype)
 
 
-def test_mid_fwd_sampled_rows(gpu, oracle_mod):
+def test_mid_fwd_all_rows(gpu, oracle_mod):
+    """The b4 s512 h32 d128 bf16 problem of "Why FlashAttention is fast",
+    every query row of every (batch, head) against the oracle."""
     w = workloads.WORKLOADS["mid_fwd"]
     q, k, v = workloads.make_workload(w)
     o, lse = run_fwd(gpu, q, k, v, w.scale)
-    # tile edges of both 128-row query tiles of each CTA, plus a spread
-    rows = sorted(set([0, 1, 127, 128, 255, 256, 383, 384, 510, 511] + list(range(3, 512, 37))))
-    o_ref, lse_ref = oracle_mod.attention(q, k, v, w.scale, rows=rows)
-    compare(o, lse, o_ref, lse_ref, rows=rows)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, w.scale)
+    compare(o, lse, o_ref, lse_ref)
+
+
+def test_several_units_per_cta_all_rows(gpu, oracle_mod):
+    """More 256-row units than SMs (b2 s1024 h48 d128: 384 units), so every
+    persistent CTA runs several units and reuses its Q buffer and O
+    accumulator; every row is compared."""
+    b, s, h, d = 2, 1024, 48, 128
+    q, k, v = workloads.make_qkv(b, s, s, h, d, torch.bfloat16, seed=29)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(gpu, q, k, v, scale)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, scale)
+    compare(o, lse, o_ref, lse_ref)
 
 
 def test_long_fwd_strided_rows(gpu, oracle_mod):

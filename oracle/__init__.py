@@ -177,7 +177,7 @@ def decode_bf16(bits: int) -> float:
     return _load().oracle_bf16_to_f64(bits)
 
 
-def paged_attention(q, k_pages, v_pages, block_table, seqlens, scale: float):
+def paged_attention(q, k_pages, v_pages, block_table, seqlens, scale: float, causal=False):
     """Exact attention of each sequence's query rows over its own keys, read
     through a page table (a paged KV cache; the pages only mention one, so
     the layout is the common one): key r of sequence i is row r % page_size
@@ -185,6 +185,10 @@ def paged_attention(q, k_pages, v_pages, block_table, seqlens, scale: float):
     seqlens[i] keys. The keys are gathered into one contiguous cache per
     sequence and passed to ``attention``; a sequence with no key gives O = 0
     and LSE = -inf.
+
+    causal: the bottom-right-aligned mask of ``attention`` taken against the
+    sequence's own key count: its sq query rows are the last sq positions of
+    its seqlens[i] keys, so row r sees key j only if j <= r + seqlens[i] - sq.
 
     q: [b, sq, h, d]; k_pages, v_pages: [num_pages, page_size, h, d];
     block_table: [b, max_pages] ints; seqlens: [b] ints (CPU tensors or
@@ -202,7 +206,12 @@ def paged_attention(q, k_pages, v_pages, block_table, seqlens, scale: float):
             keys = [int(table[i, p]) for p in range(npg)]
         kc = _stack_pages(k_pages, keys)
         vc = _stack_pages(v_pages, keys)
-        o_i, l_i = attention(q[i:i + 1], kc, vc, scale, key_range=(0, n))
+        if causal and n > 0:
+            # the mask is relative to the sequence's own keys: cut the gathered
+            # cache to exactly n keys
+            o_i, l_i = attention(q[i:i + 1], kc[:, :n], vc[:, :n], scale, causal=True)
+        else:
+            o_i, l_i = attention(q[i:i + 1], kc, vc, scale, key_range=(0, n))
         outs_o.append(o_i)
         outs_l.append(l_i)
     return np.concatenate(outs_o, axis=0), np.concatenate(outs_l, axis=0)

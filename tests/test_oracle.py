@@ -411,6 +411,39 @@ def test_paged_empty_sequence(oracle_mod):
     np.testing.assert_allclose(o[1:], o_ref, rtol=0, atol=1e-12)
 
 
+def test_paged_several_rows_equal_contiguous_cache(oracle_mod):
+    b, sq, sk, h, d, ps = 2, 5, 12, 2, 4, 4
+    q, k, v = _rand((b, sq, h, d), 49), _rand((b, sk, h, d), 50), _rand((b, sk, h, d), 51)
+    kp, vp, table = _paged_from_contiguous(k, v, ps, 3)
+    o, lse = oracle_mod.paged_attention(q, kp, vp, table, np.full(b, sk), 0.6)
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.6)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_paged_causal_is_torch_bottom_right_mask_per_sequence(oracle_mod):
+    """Several new rows per sequence under the causal mask, each sequence's
+    mask aligned to its own key count (torch fp64 SDPA with the explicit
+    bottom-right mask on the sequence's keys); rows that see no key (length
+    below sq) give O = 0 and LSE = -inf."""
+    b, sq, sk, h, d, ps = 4, 6, 16, 2, 5, 4
+    q, k, v = _rand((b, sq, h, d), 52), _rand((b, sk, h, d), 53), _rand((b, sk, h, d), 54)
+    kp, vp, table = _paged_from_contiguous(k, v, ps, 9)
+    lens = np.array([16, 7, 3, 0])
+    o, lse = oracle_mod.paged_attention(q, kp, vp, table, lens, 0.45, causal=True)
+    for i, n in enumerate(lens):
+        if n == 0:
+            assert np.all(o[i] == 0.0) and np.all(np.isneginf(lse[i]))
+            continue
+        mask = _bottom_right_mask(sq, n)
+        seen = mask.any(axis=1)
+        ro, rl = _torch_masked(q[i:i + 1], k[i:i + 1, :n], v[i:i + 1, :n], 0.45, mask)
+        np.testing.assert_allclose(o[i:i + 1, seen], ro[:, seen], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[i:i + 1, :, seen], rl[:, :, seen], rtol=0, atol=1e-12)
+        assert np.all(o[i, ~seen] == 0.0) and np.all(np.isneginf(lse[i, :, ~seen]))
+        assert (~seen).sum() == max(0, sq - n)
+
+
 # ---------------------------------------------------------------- backward pass
 # The gradients by the chain rule; pinned to torch's fp64 autograd (a library
 # special case), to finite differences of the oracle's own forward, and to

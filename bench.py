@@ -403,11 +403,22 @@ def measure_extras(ea, dev, flush, stream, peaks):
         fn = lambda: ea.attn_fwd(q, k, v, scale=w.scale)  # noqa: E731
         (ms,), _ = time_loop([fn], 20, 3, flush, stream)
         tf = w.flops / (ms * 1e-3) / 1e12
+        gbs = w.io_bytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
                      "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
-                     "GB/s": round(w.io_bytes / (ms * 1e-3) / 1e9, 1)}
+                     "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
         if name != "long_fwd":
             out[name]["host_call_us"] = host_call_us(ea, q, k, v, w, stream)
+        if name == "small_head_b512_s150":
+            # the same problem on the general key-tile-loop kernel, which the
+            # short forward (all keys of a head in one tile) replaces here
+            ea.attn_debug_set_flags(ea.ATTN_DEBUG_GENERAL_FWD)
+            try:
+                (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+            finally:
+                ea.attn_debug_set_flags(0)
+            out[name + "/general_kernel"] = {"ms": round(ms, 5),
+                                             "GB/s": round(w.io_bytes / (ms * 1e-3) / 1e9, 1)}
         del q, k, v
     # causal forward (bottom-right aligned; sq == sk here): FLOP counts only
     # the unmasked scores, 4*b*h*d * sum over rows of the keys a row sees
@@ -478,6 +489,32 @@ def measure_extras(ea, dev, flush, stream, peaks):
         out[f"{name}/paged256"] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
                                    "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
         del q, kp, vp
+    # paged KV cache with small pages: one new row per sequence, and 10 new
+    # rows (the tensor-core path, 128-key tiles gathered from 64-key pages)
+    for name in ("decode_b8_h48_sk8192", "decode_b1_h16_sk32768"):
+        w = workloads.WORKLOADS[name]
+        _, k, v = rand(w)
+        for ps in (16, 64):
+            npg = w.sk // ps
+            perm = torch.randperm(w.b * npg, generator=gen, device=dev)
+            kp = torch.empty((w.b * npg, ps, w.h, w.d), dtype=w.dtype, device=dev)
+            vp = torch.empty_like(kp)
+            kp[perm] = k.reshape(w.b * npg, ps, w.h, w.d)
+            vp[perm] = v.reshape(w.b * npg, ps, w.h, w.d)
+            table = perm.to(torch.int32).reshape(w.b, npg).contiguous()
+            lens = torch.full((w.b,), w.sk, dtype=torch.int32, device=dev)
+            kv = 2 * kp.numel() * kp.element_size()
+            for sq in (1, 10):
+                q = torch.randn((w.b, sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+                fn = lambda: ea.attn_decode_paged(q, kp, vp, table, lens,  # noqa: E731
+                                                  scale=w.scale)
+                (ms,), _ = time_loop([fn], 20, 3, flush, stream)
+                gbs = kv / (ms * 1e-3) / 1e9
+                out[f"{name}/paged{ps}/sq={sq}"] = {"ms": round(ms, 5), "GB/s (K+V)": round(gbs, 1),
+                                                    "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+                del q
+            del kp, vp, table
+        del k, v
     for name, split_list in (("decode_b8_h48_sk8192", [0]),
                              ("decode_b1_h16_sk32768", [0, 1, 2, 4, 8, 16])):
         w = workloads.WORKLOADS[name]

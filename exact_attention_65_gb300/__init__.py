@@ -30,6 +30,7 @@ ATTN_ERR_CUDA = 3
 ATTN_ERR_NO_MEMORY = 4
 ATTN_ERR_DEVICE_TIMEOUT = 5
 ATTN_DEBUG_SKIP_LOADS = 1
+ATTN_DEBUG_GENERAL_FWD = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_paged.restype = i32
         lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                           i32, f32, i32, i32, vp]
+        lib.attn_decode_paged_ex.restype = i32
+        lib.attn_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                             i32, i32, f32, i32, i32, i32, vp]
         for fn in (lib.attn_bwd, lib.attn_bwd_causal):
             fn.restype = i32
             fn.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, f32, i32, vp]
@@ -116,10 +120,8 @@ def _dtype_code(t: torch.Tensor) -> int:
     return code
 
 
-def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
-    """Sizes (b, sq, sk, h, d) and dtype code of a q, k, v triple; raises on
-    anything the C ABI would not take. Kept lean: small problems issue in a
-    few microseconds, and this runs on every call."""
+def _check_slow(q, k, v):
+    """Raises the specific error for a q, k, v triple _check refused."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
@@ -127,28 +129,46 @@ def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
             raise ValueError(f"{name} must be [b, s, h, d], got shape {tuple(t.shape)}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous in (b, s, h, d) order")
+    raise ValueError("invalid q, k, v")
+
+
+def _check(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    """Sizes (b, sq, sk, h, d), dtype code and device index of a q, k, v
+    triple; raises on anything the C ABI would not take. Kept lean: small
+    problems issue in a few microseconds, and this runs on every call."""
+    try:
+        ok = (q.is_cuda and k.is_cuda and v.is_cuda and q.dim() == 4 and k.dim() == 4
+              and v.dim() == 4 and q.is_contiguous() and k.is_contiguous() and v.is_contiguous())
+    except AttributeError:
+        ok = False
+    if not ok:
+        _check_slow(q, k, v)
     dt = q.dtype
     if k.dtype is not dt or v.dtype is not dt:
         raise TypeError("q, k, v must share one dtype")
-    dev = q.device
-    if k.device != dev or v.device != dev:
+    idx = q.get_device()
+    if k.get_device() != idx or v.get_device() != idx:
         raise ValueError("q, k, v must be on the same device")
     b, sq, h, d = q.shape
     kb, sk, kh, kd = k.shape
     if kb != b or kh != h or kd != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
-    return b, sq, sk, h, d, _dtype_code(q)
+    code = _DTYPE_CODE.get(dt)
+    if code is None:
+        raise TypeError(f"exattn takes float16 or bfloat16 tensors, got {dt}")
+    return b, sq, sk, h, d, code, idx
 
 
-def _outputs(q, out, lse, b, h, sq):
+def _outputs(q, out, lse, b, h, sq, idx):
     if out is None:
         out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+    elif (out.shape != q.shape or out.dtype is not q.dtype or not out.is_contiguous()
+          or out.get_device() != idx):
         raise ValueError("out must be a contiguous tensor like q")
     if lse is None:
         lse = torch.empty((b, h, sq), dtype=torch.float32, device=q.device)
-    elif (lse.shape != (b, h, sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
-          or lse.device != q.device):
+    elif (lse.shape != (b, h, sq) or lse.dtype is not torch.float32 or not lse.is_contiguous()
+          or lse.get_device() != idx):
         raise ValueError("lse must be a contiguous float32 tensor [b, h, sq]")
     return out, lse
 
@@ -159,14 +179,14 @@ def _stream(device, stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _call(fn, device, stream, *args):
-    """Call C-ABI function ``fn`` with ``args`` plus the stream, with
-    ``device`` current. The common case (device already current, its current
+def _call(fn, idx, stream, *args):
+    """Call C-ABI function ``fn`` with ``args`` plus the stream, with device
+    ``idx`` current. The common case (device already current, its current
     stream) skips the device context manager and the Stream object."""
-    idx = device.index
     if idx == _current_device():
         raw = _current_raw_stream(idx) if stream is None else stream.cuda_stream
         return fn(*args, raw)
+    device = torch.device("cuda", idx)
     with torch.cuda.device(device):
         return fn(*args, _stream(device, stream))
 
@@ -179,12 +199,12 @@ def attn_fwd(q, k, v, scale: float | None = None, out=None, lse=None, stream=Non
     tensors; default scale 1/sqrt(d). Runs on ``stream`` (default: the
     current stream of q's device). ``causal``: bottom-right-aligned mask
     (query row i sees key j only if j <= i + sk - sq)."""
-    b, sq, sk, h, d, dt = _check(q, k, v)
+    b, sq, sk, h, d, dt, idx = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    out, lse = _outputs(q, out, lse, b, h, sq)
+    out, lse = _outputs(q, out, lse, b, h, sq, idx)
     lib = _lib or load_library()
     fn = lib.attn_fwd_causal if causal else lib.attn_fwd
-    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+    rc = _call(fn, idx, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                lse.data_ptr(), b, sq, sk, h, d, scale, dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_causal" if causal else "attn_fwd")
@@ -242,12 +262,12 @@ def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0
     """Split-KV decode: same result as attn_fwd, computed by splitting the
     keys into ``num_splits`` ranges (0 = heuristic) and reducing the
     per-split (O_i, LSE_i) with the log-sum-exp combine."""
-    b, sq, sk, h, d, dt = _check(q, k, v)
+    b, sq, sk, h, d, dt, idx = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    out, lse = _outputs(q, out, lse, b, h, sq)
+    out, lse = _outputs(q, out, lse, b, h, sq, idx)
     lib = _lib or load_library()
     fn = lib.attn_decode_splitkv_causal if causal else lib.attn_decode_splitkv_ex
-    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+    rc = _call(fn, idx, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                lse.data_ptr(), b, sq, sk, h, d, scale, int(num_splits), dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_splitkv")
@@ -255,14 +275,16 @@ def attn_decode_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0
 
 
 def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float | None = None,
-                      num_splits: int = 0, out=None, lse=None, stream=None):
-    """Split-KV decode of one new row per sequence from a paged KV cache.
+                      num_splits: int = 0, out=None, lse=None, stream=None, causal: bool = False):
+    """Split-KV decode of the new rows of each sequence from a paged KV cache.
 
-    q: [b, 1, h, d]; k_pages, v_pages: [num_pages, page_size, h, d] (page_size
-    a multiple of 256); block_table: int32 [b, max_pages] pool page of each
-    logical page; seqlens_k: int32 [b] keys per sequence. All CUDA tensors."""
-    if not isinstance(q, torch.Tensor) or not q.is_cuda or q.dim() != 4 or q.shape[1] != 1:
-        raise ValueError("q must be a CUDA tensor [b, 1, h, d]")
+    q: [b, sq, h, d] (sq new rows per sequence); k_pages, v_pages:
+    [num_pages, page_size, h, d] (page_size a multiple of 16); block_table:
+    int32 [b, max_pages] pool page of each logical page; seqlens_k: int32
+    [b] keys per sequence. All CUDA tensors. ``causal``: the
+    bottom-right-aligned mask against each sequence's own key count."""
+    if not isinstance(q, torch.Tensor) or not q.is_cuda or q.dim() != 4:
+        raise ValueError("q must be a CUDA tensor [b, sq, h, d]")
     for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor [num_pages, page_size, h, d]")
@@ -276,7 +298,7 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float 
             raise ValueError(f"{name} must be a contiguous int32 CUDA tensor on q's device")
     if not q.is_contiguous():
         raise ValueError("q must be contiguous")
-    b, _, h, d = q.shape
+    b, sq, h, d = q.shape
     num_pages, page_size = k_pages.shape[0], k_pages.shape[1]
     if k_pages.shape[2] != h or k_pages.shape[3] != d:
         raise ValueError("page pools must be [num_pages, page_size, h, d] with q's h and d")
@@ -284,12 +306,13 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale: float 
         raise ValueError("block_table must be [b, max_pages] and seqlens_k [b]")
     dt = _dtype_code(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    out, lse = _outputs(q, out, lse, b, h, 1)
+    idx = q.get_device()
+    out, lse = _outputs(q, out, lse, b, h, sq, idx)
     lib = _lib or load_library()
-    rc = _call(lib.attn_decode_paged, q.device, stream, q.data_ptr(), k_pages.data_ptr(),
+    rc = _call(lib.attn_decode_paged_ex, idx, stream, q.data_ptr(), k_pages.data_ptr(),
                v_pages.data_ptr(), block_table.data_ptr(), seqlens_k.data_ptr(), out.data_ptr(),
-               lse.data_ptr(), b, h, d, num_pages, page_size, block_table.shape[1], scale,
-               int(num_splits), dt)
+               lse.data_ptr(), b, sq, h, d, num_pages, page_size, block_table.shape[1], scale,
+               int(num_splits), 1 if causal else 0, dt)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged")
     return out, lse
@@ -302,7 +325,7 @@ def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None
     q, o, dout: [b, sq, h, d]; k, v: [b, sk, h, d] (fp16 or bf16, contiguous
     CUDA tensors); lse: fp32 [b, h, sq] from attn_fwd with the same
     ``causal`` (the bottom-right-aligned mask, attn_bwd_causal)."""
-    b, sq, sk, h, d, dt = _check(q, k, v)
+    b, sq, sk, h, d, dt, idx = _check(q, k, v)
     for name, t in (("o", o), ("dout", dout)):
         if not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != q.dtype \
                 or not t.is_contiguous() or t.device != q.device:
@@ -319,7 +342,7 @@ def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, dq=None, dk=None
             raise ValueError(f"{name} must be a contiguous tensor like {name[1]}")
     lib = _lib or load_library()
     fn = lib.attn_bwd_causal if causal else lib.attn_bwd
-    rc = _call(fn, q.device, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+    rc = _call(fn, idx, stream, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                b, sq, sk, h, d, scale, dt)
     if rc != ATTN_OK:
@@ -333,13 +356,13 @@ def attn_decode_splitkv_noalloc(q, k, v, out, lse, scale: float | None = None,
     out and lse must be given, and the per-split partials live in a fixed
     array inside the library (calls that overlap on the GPU race on it).
     Its kernels' timeouts are read by attn_get_noalloc_status()."""
-    b, sq, sk, h, d, dt = _check(q, k, v)
+    b, sq, sk, h, d, dt, idx = _check(q, k, v)
     if out is None or lse is None:
         raise ValueError("out and lse must be given: this entry point allocates nothing")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    out, lse = _outputs(q, out, lse, b, h, sq)
+    out, lse = _outputs(q, out, lse, b, h, sq, idx)
     lib = _lib or load_library()
-    rc = _call(lib.attn_decode_splitkv_noalloc, q.device, stream, q.data_ptr(), k.data_ptr(),
+    rc = _call(lib.attn_decode_splitkv_noalloc, idx, stream, q.data_ptr(), k.data_ptr(),
                v.data_ptr(), out.data_ptr(), lse.data_ptr(), b, sq, sk, h, d, scale,
                int(num_splits), dt)
     if rc != ATTN_OK:

@@ -278,6 +278,45 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     const int box0 = fwd_row_bytes(d) / 2;
     CUtensorMap tq, tk, tv;
+    // Short key sequences with small heads (every key of a head in one tile,
+    // several tiles in flight per SM): the short forward.
+    ShortArgs sa;
+    if (splits == 1 && !causal && !(debug_flags() & kFlagGeneralFwd) && short_plan(sk, d, &sa)) {
+        const int64_t items = cdiv(sq, SHORT_BM) * h * b;
+        if (items > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+        if (!encode_4d(&tq, q, bf16, d, h, sq, b, d, SHORT_BM, fwd_swizzle(d)) ||
+            !encode_4d(&tk, k, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d)) ||
+            !encode_4d(&tv, v, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d)))
+            return ATTN_ERR_CUDA;
+        sa.o = o;
+        sa.lse = lse;
+        sa.b = b;
+        sa.sq = sq;
+        sa.sk = sk;
+        sa.h = h;
+        sa.scale_log2 = scale * kLog2e;
+        sa.status = ds->status;
+        sa.flags = debug_flags();
+        // CTA c takes items c, c + grid, c + 2 grid, ...; a grid that shares
+        // no factor with the tiles per head deals every CTA each tile index
+        // in turn (with 2 tiles per head and 152 CTAs, half of the CTAs would
+        // get only full first tiles and the other half only short last ones)
+        const int64_t ntile = cdiv(sq, SHORT_BM);
+        int64_t grid = items < ds->num_sms ? items : ds->num_sms;
+        auto gcd = [](int64_t x, int64_t y) {
+            while (y) {
+                const int64_t t = x % y;
+                x = y;
+                y = t;
+            }
+            return x;
+        };
+        while (grid > 1 && items > grid && gcd(grid, ntile) != 1) --grid;
+        return launch_fwd_short(d, bf16, tq, tk, tv, sa, static_cast<int>(grid), stream) ==
+                       cudaSuccess
+                   ? ATTN_OK
+                   : ATTN_ERR_CUDA;
+    }
     if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, FWD_BM, fwd_swizzle(d)) ||
         !encode_4d(&tk, k, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)) ||
         !encode_4d(&tv, v, bf16, d, h, sk, b, box0, FWD_BN, fwd_swizzle(d)))
@@ -299,6 +338,74 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     a.lse_part = nullptr;
     a.causal = causal ? 1 : 0;
     a.longest_first = causal ? 1 : 0;
+    if (splits == 1)
+        return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    void *ws = nullptr;
+    attn_status_t st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, stream);
+    if (e == cudaSuccess)
+        e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Several new query rows per sequence from a paged cache: the tensor-core
+// forward kernel over key ranges of whole 128-key tiles, its K/V tiles
+// gathered through the block table in boxes of at most a page, with fp32
+// partials reduced by the combine kernel when there is more than one split.
+// Splits are chosen for the longest sequence the table allows (the lengths
+// live on the device); splits past a sequence's end are empty.
+attn_status_t run_fwd_paged(const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *block_table, const int32_t *seqlens, void *o,
+                            float *lse, int b, int sq, int h, int d, int num_pages, int page_size,
+                            int max_pages, float scale, int num_splits, bool causal, bool bf16,
+                            const DeviceState *ds, cudaStream_t stream) {
+    const int64_t sk_max = static_cast<int64_t>(max_pages) * page_size;
+    const int64_t nkv = cdiv(sk_max, FWD_BN);
+    int64_t splits =
+        num_splits == 0
+            ? attn_decode_num_splits_for_sms(b, sq, static_cast<int>(sk_max), h, d, ds->num_sms)
+            : num_splits;
+    if (splits > nkv) splits = nkv;
+    if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
+    if (splits < 1) splits = 1;
+    const int64_t tps = cdiv(nkv, splits);
+    splits = cdiv(nkv, tps);
+    if (cdiv(sq, FWD_BM * FWD_QTILES) * splits * h * b > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    // boxes: the largest power of two that divides the page and the tile
+    int box_rows = FWD_BN;
+    while (page_size % box_rows != 0) box_rows /= 2;
+    const int box0 = fwd_row_bytes(d) / 2;
+    CUtensorMap tq, tk, tv;
+    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, FWD_BM, fwd_swizzle(d)) ||
+        !encode_4d(&tk, k_pages, bf16, d, h, page_size, num_pages, box0, box_rows,
+                   fwd_swizzle(d)) ||
+        !encode_4d(&tv, v_pages, bf16, d, h, page_size, num_pages, box0, box_rows, fwd_swizzle(d)))
+        return ATTN_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.b = b;
+    a.sq = sq;
+    a.sk = static_cast<int>(sk_max);
+    a.h = h;
+    a.scale_log2 = scale * kLog2e;
+    a.status = ds->status;
+    a.flags = debug_flags();
+    a.num_sms = ds->num_sms;
+    a.splits = static_cast<int>(splits);
+    a.tiles_per_split = static_cast<int>(tps);
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    a.causal = causal ? 1 : 0;
+    a.longest_first = causal ? 1 : 0;
+    a.block_table = block_table;
+    a.seqlens = seqlens;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.box_rows = box_rows;
     if (splits == 1)
         return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     void *ws = nullptr;
@@ -349,7 +456,9 @@ const char *attn_status_string(attn_status_t s) {
     return "unknown status";
 }
 
-void attn_debug_set_flags(unsigned int flags) { g_flags = flags & ATTN_DEBUG_SKIP_LOADS; }
+void attn_debug_set_flags(unsigned int flags) {
+    g_flags = flags & (ATTN_DEBUG_SKIP_LOADS | ATTN_DEBUG_GENERAL_FWD);
+}
 
 unsigned int attn_last_timeout_site(void) { return g_last_site; }
 
@@ -682,29 +791,35 @@ attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const voi
                    stream);
 }
 
-attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
-                                const int32_t *block_table, const int32_t *seqlens_k, void *o,
-                                float *lse, int b, int h, int d, int num_pages, int page_size,
-                                int max_pages_per_seq, float scale, int num_splits,
-                                attn_dtype_t dtype, cudaStream_t stream) {
+attn_status_t attn_decode_paged_ex(const void *q, const void *k_pages, const void *v_pages,
+                                   const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                                   float *lse, int b, int sq, int h, int d, int num_pages,
+                                   int page_size, int max_pages_per_seq, float scale,
+                                   int num_splits, int causal, attn_dtype_t dtype,
+                                   cudaStream_t stream) {
     if (!block_table || !seqlens_k || !aligned(block_table, 4) || !aligned(seqlens_k, 4))
         return ATTN_ERR_INVALID_ARG;
     if (num_pages < 1 || page_size < 1 || max_pages_per_seq < 1 || num_splits < 0)
         return ATTN_ERR_INVALID_ARG;
-    // a TMA box of the decode kernel (up to 256 key rows) never crosses a page
-    if (page_size % 256 != 0) return ATTN_ERR_UNSUPPORTED;
+    // TMA boxes of at most a page: page sizes are multiples of 16 keys
+    if (page_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     const int64_t sk_max = static_cast<int64_t>(max_pages_per_seq) * page_size;
     if (sk_max > 0x7fffffffLL || static_cast<int64_t>(b) * max_pages_per_seq > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
-    // q [b, 1, h, d]; the pools stand in for k and v in the common checks
-    attn_status_t st = validate_args(q, k_pages, v_pages, o, lse, b, 1, static_cast<int>(sk_max),
+    // q [b, sq, h, d]; the pools stand in for k and v in the common checks
+    attn_status_t st = validate_args(q, k_pages, v_pages, o, lse, b, sq, static_cast<int>(sk_max),
                                      h, d, scale, dtype);
     if (st != ATTN_OK) return st;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     const bool bf16 = dtype == ATTN_BF16;
-    // The lengths live on the device: splits are chosen for the longest
-    // sequence the table allows; splits past a sequence's end are empty.
+    if (sq > 1) return run_fwd_paged(q, k_pages, v_pages, block_table, seqlens_k, o, lse, b, sq, h,
+                                     d, num_pages, page_size, max_pages_per_seq, scale, num_splits,
+                                     causal != 0, bf16, ds, stream);
+    // One new row per sequence (which sees every key under the causal mask):
+    // the CUDA-core split kernel. The lengths live on the device, so splits
+    // are chosen for the longest sequence the table allows; splits past a
+    // sequence's end are empty.
     const int64_t nblocks = cdiv(sk_max, dec_block_rows(d));
     int64_t splits = num_splits == 0
                          ? dec_num_splits(b, 1, static_cast<int>(sk_max), h, d, ds->num_sms)
@@ -713,10 +828,13 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
     if (splits < 1) splits = 1;
 
+    // the largest power of two that divides the page and fits the kernel's box
+    int box_rows = dec_box_rows(d);
+    while (page_size % box_rows != 0) box_rows /= 2;
     CUtensorMap tk, tv;
-    if (!encode_4d(&tk, k_pages, bf16, d, h, page_size, num_pages, d, dec_box_rows(d),
+    if (!encode_4d(&tk, k_pages, bf16, d, h, page_size, num_pages, d, box_rows,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_4d(&tv, v_pages, bf16, d, h, page_size, num_pages, d, dec_box_rows(d),
+        !encode_4d(&tv, v_pages, bf16, d, h, page_size, num_pages, d, box_rows,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
         return ATTN_ERR_CUDA;
     DecodeArgs a;
@@ -739,9 +857,20 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     a.page_size = page_size;
     a.max_pages = max_pages_per_seq;
     a.num_pages = num_pages;
+    a.box_rows = box_rows;
     if (splits == 1)
         return launch_decode(d, bf16, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     return run_split_decode(ds, d, bf16, tk, tv, a, stream);
+}
+
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                                float *lse, int b, int h, int d, int num_pages, int page_size,
+                                int max_pages_per_seq, float scale, int num_splits,
+                                attn_dtype_t dtype, cudaStream_t stream) {
+    return attn_decode_paged_ex(q, k_pages, v_pages, block_table, seqlens_k, o, lse, b, 1, h, d,
+                                num_pages, page_size, max_pages_per_seq, scale, num_splits, 0,
+                                dtype, stream);
 }
 
 attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,

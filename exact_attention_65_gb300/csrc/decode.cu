@@ -455,22 +455,25 @@ __global__ void __launch_bounds__(DecGeom<D, ST>::THREADS)
                 if (!mbar_wait(empty(s), ph ^ 1, g, 1)) break;
                 mbar_arrive_expect_tx(full(s), G::STAGE_BYTES);
                 const uint32_t dst = sbase + s * G::STAGE_BYTES;
-#pragma unroll
-                for (int x = 0; x < G::BOXES; ++x) {
-                    int r = blk * G::BN + x * G::BOX_ROWS;
+                // a paged cache's boxes are at most a page high (box_rows, a
+                // power of two dividing page_size), so none crosses a page
+                const int box_rows = PAGED ? a.box_rows : G::BOX_ROWS;
+                const int boxes = PAGED ? G::BN / box_rows : G::BOXES;
+#pragma unroll 4
+                for (int x = 0; x < boxes; ++x) {
+                    int r = blk * G::BN + x * box_rows;
                     int outer = batch;
                     if constexpr (PAGED) {
-                        // A box never crosses a page (page_size is a multiple of
-                        // 256). Rows past the sequence's end are masked by the
+                        // Rows past the sequence's end are masked by the
                         // consumers; their page index is only kept in range.
                         const int lp = min(r / a.page_size, a.max_pages - 1);
                         const int pg = a.block_table[static_cast<int64_t>(batch) * a.max_pages + lp];
                         outer = min(max(pg, 0), a.num_pages - 1);
                         r -= lp * a.page_size;
                     }
-                    tma_load_4d_hint(dst + x * G::BOX_ROWS * D * 2, &tk, full(s), 0, head, r, outer,
+                    tma_load_4d_hint(dst + x * box_rows * D * 2, &tk, full(s), 0, head, r, outer,
                                      stream_once);
-                    tma_load_4d_hint(dst + G::BLOCK_BYTES + x * G::BOX_ROWS * D * 2, &tv, full(s), 0,
+                    tma_load_4d_hint(dst + G::BLOCK_BYTES + x * box_rows * D * 2, &tv, full(s), 0,
                                      head, r, outer, stream_once);
                 }
             }

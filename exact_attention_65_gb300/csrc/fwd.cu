@@ -78,9 +78,10 @@ struct FwdGeom {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + QBUF * Q_BUF_BYTES;
     static constexpr int OFF_BAR = OFF_KV + SLOTS * KV_TILE_BYTES;
-    // barriers: q_full | q_empty | kv_full[SLOTS] | kv_empty[SLOTS] |
-    //           s_full[QT] | p_full[QT] | o_full[QT] | o_empty[QT] | done
-    static constexpr int BAR_QF = 0;            // [QBUF]
+    // barriers: q_full[QBUF] | q_empty[QBUF] | kv_full[SLOTS] |
+    //           kv_empty[SLOTS] | s_full[QT] | p_full[QT] | o_full[QT] |
+    //           o_empty[QT] | done | v_land | v_fix
+    static constexpr int BAR_QF = 0;              // [QBUF]
     static constexpr int BAR_QE = BAR_QF + QBUF;  // [QBUF]
     static constexpr int BAR_KVF = BAR_QE + QBUF;
     static constexpr int BAR_KVE = BAR_KVF + SLOTS;
@@ -89,7 +90,9 @@ struct FwdGeom {
     static constexpr int BAR_OF = BAR_PF + QT;
     static constexpr int BAR_OE = BAR_OF + QT;
     static constexpr int BAR_DONE = BAR_OE + QT;
-    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int BAR_VLAND = BAR_DONE + 1;  // paged: last V tile landed (MMA -> zeroing)
+    static constexpr int BAR_VFIX = BAR_VLAND + 1;  // paged: its stale rows zeroed (zeroing -> MMA)
+    static constexpr int NUM_BARS = BAR_VFIX + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int USED = OFF_MISC + 16;
     // Keep one CTA per SM: it owns all 512 TMEM columns.
@@ -120,12 +123,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // two 128-row tiles hold rows below sq.
 struct Unit {
     int m0, head, batch, n_qt, split, kv0, nkv;
+    int sk;  // keys of this unit's sequence (a.sk unless the cache is paged)
 };
 
 // Units are numbered query block first, then split, head and batch. The
 // kernel is compiled with and without key splits (SPLIT): the plain forward
 // keeps the shorter code.
-template <bool SPLIT>
+template <bool SPLIT, bool PAGED>
 __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdArgs &a) {
     Unit x;
     int qb = u % nqb;
@@ -148,14 +152,21 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     x.split = 0;
     x.kv0 = 0;
     x.nkv = nkv_all;
+    x.sk = a.sk;
     if constexpr (SPLIT) {
         x.split = r % a.splits;
         r /= a.splits;
-        x.kv0 = x.split * a.tiles_per_split;
-        x.nkv = min(a.tiles_per_split, nkv_all - x.kv0);
     }
     x.head = r % a.h;
     x.batch = r / a.h;
+    if constexpr (SPLIT) {
+        if constexpr (PAGED) {  // the sequence's own length, on the device
+            x.sk = min(max(__ldg(a.seqlens + x.batch), 0), a.sk);
+            nkv_all = (x.sk + FWD_BN - 1) / FWD_BN;
+        }
+        x.kv0 = x.split * a.tiles_per_split;
+        x.nkv = max(0, min(a.tiles_per_split, nkv_all - x.kv0));
+    }
     x.m0 = qb * (FWD_BM * FWD_QTILES);
     x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
     if constexpr (SPLIT) {
@@ -163,7 +174,7 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
             // the unit's last row sees keys up to last + sk - sq: later key
             // tiles are not needed (none at all if that is below 0)
             const int last = min(x.m0 + FWD_BM * FWD_QTILES, a.sq) - 1;
-            const int kmax = last + a.sk - a.sq;
+            const int kmax = last + x.sk - a.sq;
             const int tiles = kmax < 0 ? 0 : kmax / FWD_BN + 1;
             x.nkv = max(0, min(x.nkv, tiles - x.kv0));
         }
@@ -171,7 +182,7 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     return x;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                              const CUtensorMap *tv, uint32_t sbase, int nqb,
                                              int units, int nkv, const FwdArgs &a,
@@ -185,7 +196,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
     int q_issued = 0, n_issued = 0;  // n counts ring items (K and V tiles)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
         // A Q buffer is free once every S MMA of the unit two back has completed.
         const int qb = q_issued % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QE + qb), ((q_issued / G::QBUF) & 1) ^ 1, g, 1)) break;
@@ -206,10 +217,35 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
             }
             mbar_arrive_expect_tx(bar(G::BAR_KVF + s), G::KV_TILE_BYTES);
             const CUtensorMap *map = (i & 1) ? tv : tk;
-            for (int p = 0; p < G::PANELS; ++p)
-                tma_load_4d_hint(sbase + G::OFF_KV + s * G::KV_TILE_BYTES + p * G::KV_PANEL_BYTES,
-                                 map, bar(G::BAR_KVF + s), p * G::PANEL_ELEMS, x.head,
-                                 (x.kv0 + (i >> 1)) * G::BN, x.batch, keep);
+            const uint32_t dst = sbase + G::OFF_KV + s * G::KV_TILE_BYTES;
+            const int row0 = (x.kv0 + (i >> 1)) * G::BN;
+            if constexpr (PAGED) {
+                // Paged: boxes of box_rows rows, each inside one page (looked
+                // up in the block table). A box wholly past the sequence's end
+                // is addressed past the last pool page, so TMA fills it with
+                // zeros; rows past the end inside the last box hold stale data
+                // (masked for K, zeroed for V before the P V MMA).
+                for (int r = 0; r < G::BN; r += a.box_rows) {
+                    const int key = row0 + r;
+                    int page = a.num_pages, prow = 0;
+                    if (key < x.sk) {
+                        const int lp = key / a.page_size;
+                        page = min(max(__ldg(a.block_table +
+                                             static_cast<int64_t>(x.batch) * a.max_pages + lp),
+                                       0),
+                                   a.num_pages - 1);
+                        prow = key - lp * a.page_size;
+                    }
+                    for (int p = 0; p < G::PANELS; ++p)
+                        tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES + r * G::ROW_BYTES, map,
+                                         bar(G::BAR_KVF + s), p * G::PANEL_ELEMS, x.head, prow,
+                                         page, keep);
+                }
+            } else {
+                for (int p = 0; p < G::PANELS; ++p)
+                    tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES, map, bar(G::BAR_KVF + s),
+                                     p * G::PANEL_ELEMS, x.head, row0, x.batch, keep);
+            }
             ++n_issued;
         }
     }
@@ -224,7 +260,59 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
         mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
 }
 
-template <int D, bool BF16, bool SPLIT>
+// Paged caches: a unit's last K/V tile can end inside the sequence's last
+// page, whose rows past the end hold stale data. P is exactly 0 there, but the
+// tensor core still multiplies those V rows (0 * NaN is NaN), so warps 2-3
+// zero them in shared memory (whole swizzled rows: a row's bytes stay in its
+// own 16-byte-chunk group under every swizzle mode). The MMA issuer, which
+// consumes the ring in order, tells them when that V tile has landed
+// (BAR_VLAND; waiting on the ring's own barrier from here could match an
+// older phase of the same parity), and they hand the tile back through
+// BAR_VFIX before its P V reads it.
+template <bool PAGED>
+__device__ __forceinline__ bool unit_needs_v_fix(const Unit &x) {
+    return PAGED && x.nkv > 0 && (x.kv0 + x.nkv) * FWD_BN > x.sk;
+}
+
+template <int D, bool SPLIT, bool PAGED>
+__device__ __forceinline__ void fwd_fix_v(uint32_t sbase, int nqb, int units, int nkv,
+                                          const FwdArgs &a, const WaitGuard &g) {
+    using G = FwdGeom<D>;
+    auto bar = [&](int i) { return sbase + 8u * i + G::OFF_BAR; };
+    const int t = threadIdx.x - 64;  // warps 2-3
+    const uint32_t lane = threadIdx.x & 31;
+    constexpr int CPR = G::ROW_BYTES / 16;  // 16-byte chunks per row and panel
+    int kv_base = 0;
+    int fix_cnt = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
+        if (unit_needs_v_fix<PAGED>(x)) {
+            const int nv = 2 * (kv_base + x.nkv - 1) + 1;  // ring item of the last V tile
+            const int slot = nv % G::SLOTS;
+            // The issuer has seen the tile land and holds the slot until the
+            // hand-back, so the ring barrier's current phase is this item's.
+            bool ok = mbar_wait(bar(G::BAR_VLAND), fix_cnt & 1, g, 15);
+            ok = ok && mbar_wait(bar(G::BAR_KVF + slot), (nv / G::SLOTS) & 1, g, 16);
+            ++fix_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            const int valid = x.sk - (x.kv0 + x.nkv - 1) * G::BN;  // 1 .. BN - 1
+            const int per_panel = (G::BN - valid) * CPR;
+            const uint32_t base = sbase + G::OFF_KV + slot * G::KV_TILE_BYTES;
+            for (int c = t; c < per_panel * G::PANELS; c += 64) {
+                const int p = c / per_panel;
+                const int rem = c - p * per_panel;
+                st_shared_zero16(base + p * G::KV_PANEL_BYTES + (valid + rem / CPR) * G::ROW_BYTES +
+                                 (rem % CPR) * 16);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(G::BAR_VFIX));
+        }
+        kv_base += x.nkv;
+    }
+}
+
+template <int D, bool BF16, bool SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, int units,
                                         int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
@@ -244,9 +332,10 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     int kv_base = 0;  // K/V tiles consumed before the current unit
     int p_cnt[G::QT] = {};  // P phases consumed per query tile
     int o_cnt[G::QT] = {};  // units finished per query tile
+    int fix_cnt = 0;        // paged V tiles handed over by the zeroing warps
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
-        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
         const int qbuf = it_u % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QF + qbuf), (it_u / G::QBUF) & 1, g, 4)) break;
         // The issue order keeps the tensor core's short instruction queue fed:
@@ -256,6 +345,14 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
             // ring items: K_j is item 2 (kv_base + j), V_{j-1} the item before it
             const int nk = 2 * (kv_base + j), nv = nk - 1;
             const int ks = nk % G::SLOTS, vs = nv % G::SLOTS;
+            // a paged unit's last V tile, once its stale rows are zeroed
+            if (j == x.nkv && unit_needs_v_fix<PAGED>(x)) {
+                if (!mbar_wait(bar(G::BAR_VFIX), fix_cnt & 1, g, 11)) {
+                    ok = false;
+                    break;
+                }
+                ++fix_cnt;
+            }
             for (int t = 0; t < x.n_qt; ++t) {
                 const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE;
                 const uint32_t tO = tS + G::TMEM_O_OFF;
@@ -315,6 +412,8 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                 ok = false;
                 break;
             }
+            // a paged unit's last V tile has landed: the zeroing warps may go
+            if (j == x.nkv - 1 && unit_needs_v_fix<PAGED>(x)) mbar_arrive(bar(G::BAR_VLAND));
         }
         // a unit with no key tile (causal) still frees its Q buffer
         if constexpr (SPLIT)
@@ -330,7 +429,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
 }
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4, int nqb,
                                             int units, int nkv, const FwdArgs &a,
                                             const WaitGuard &g) {
@@ -345,7 +444,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     int s_cnt = 0, o_cnt = 0;
 
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit x = unit_of<SPLIT>(u, nqb, nkv, a);
+        const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
         if (t >= x.n_qt) continue;
         const int tile_row0 = x.m0 + t * G::BM;
         const int grow = tile_row0 + row;
@@ -368,12 +467,12 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 // keys of this tile the row may use: inside [0, sk) and, with the
                 // causal mask, at most grow + sk - sq. Loads and chunk skips
                 // follow the warp's largest count (tcgen05.ld is warp-wide).
-                int valid = a.sk - (x.kv0 + j) * G::BN;
+                int valid = x.sk - (x.kv0 + j) * G::BN;
                 int vmax = valid;
                 bool ragged = valid < G::BN;
                 if constexpr (SPLIT) {
                     if (a.causal) {
-                        valid = min(valid, grow + a.sk - a.sq + 1 - (x.kv0 + j) * G::BN);
+                        valid = min(valid, grow + x.sk - a.sq + 1 - (x.kv0 + j) * G::BN);
                         vmax = __reduce_max_sync(0xffffffffu, valid);
                         ragged = __any_sync(0xffffffffu, valid < G::BN);
                     }
@@ -596,7 +695,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     }
 }
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool PAGED>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -623,6 +722,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if ((i >= G::BAR_PF && i < G::BAR_PF + G::QT) ||
                 (i >= G::BAR_OE && i < G::BAR_OE + G::QT))
                 count = 4;
+            if (i == G::BAR_VFIX) count = 2;  // one arrive per zeroing warp
             mbar_init(bar(i), count);
         }
         *abort_flag = 0u;
@@ -647,13 +747,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         reg_dealloc<kRegsControl>();
         if (warp == 0) {
             if (lane == 0 && !(a.flags & kFlagSkipLoads))
-                fwd_producer<D, SPLIT>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+                fwd_producer<D, SPLIT, PAGED>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
         } else if (warp == 1) {
-            if (lane == 0) fwd_mma<D, BF16, SPLIT>(sbase, tmem, nqb, units, nkv, a, g);
+            if (lane == 0) fwd_mma<D, BF16, SPLIT, PAGED>(sbase, tmem, nqb, units, nkv, a, g);
+        } else if (PAGED && !(a.flags & kFlagSkipLoads)) {
+            fwd_fix_v<D, SPLIT, PAGED>(sbase, nqb, units, nkv, a, g);
         }
     } else {
         reg_alloc<kRegsSoftmax>();
-        fwd_softmax<D, BF16, SPLIT>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv, a, g);
+        fwd_softmax<D, BF16, SPLIT, PAGED>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv,
+                                           a, g);
     }
 
     tc_fence_before();
@@ -662,7 +765,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool PAGED>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
     using G = FwdGeom<D>;
@@ -671,7 +774,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_kernel<D, BF16, SPLIT>,
+        e = cudaFuncSetAttribute(fwd_kernel<D, BF16, SPLIT, PAGED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -686,7 +789,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     const int64_t waves = (units + a.num_sms - 1) / a.num_sms;
     const int64_t ctas =
         a.causal ? (units < a.num_sms ? units : a.num_sms) : (units + waves - 1) / waves;
-    fwd_kernel<D, BF16, SPLIT>
+    fwd_kernel<D, BF16, SPLIT, PAGED>
         <<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
@@ -694,8 +797,11 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 template <int D, bool BF16>
 cudaError_t launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
-    return (a.splits > 1 || a.causal) ? launch_fwd_t<D, BF16, true>(tq, tk, tv, a, stream)
-                                      : launch_fwd_t<D, BF16, false>(tq, tk, tv, a, stream);
+    // three instantiations: the plain forward, key ranges / causal, and key
+    // ranges over a paged cache; each keeps only the code it needs
+    if (a.block_table) return launch_fwd_t<D, BF16, true, true>(tq, tk, tv, a, stream);
+    return (a.splits > 1 || a.causal) ? launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, stream)
+                                      : launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, stream);
 }
 
 }  // namespace

@@ -44,10 +44,55 @@ struct FwdArgs {
     // Causal units in longest-first order across all (batch, head) pairs,
     // instead of alternating the query-block order per (batch, head).
     int longest_first;
+    // Paged K/V (block_table != nullptr; key-split instantiation only): the
+    // K/V maps cover page pools [num_pages, page_size, h, d]; key row r of
+    // sequence bb is row r % page_size of pool page
+    // block_table[bb * max_pages + r / page_size], and the sequence has
+    // seqlens[bb] keys (sk is then max_pages * page_size, the most it may
+    // have; the causal mask is aligned to each sequence's own count). K/V
+    // tiles are loaded as boxes of box_rows rows, a power of two dividing
+    // both page_size and the 128-key tile.
+    const int32_t *block_table = nullptr;
+    const int32_t *seqlens = nullptr;
+    int page_size = 0;
+    int max_pages = 0;
+    int num_pages = 0;
+    int box_rows = 0;
 };
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdArgs &a, cudaStream_t stream);
+
+// ------------------------------------------------------------ short forward
+// Forward for sk <= SHORT_MAX_KEYS and d <= 64 (fwd_short.cu): one work item
+// is a 128-row query tile of one (batch, head) against all of its keys, and
+// up to SHORT_MAX_SLOTS items are in flight per SM, one per TMEM slot.
+constexpr int SHORT_BM = 128;
+constexpr int SHORT_MAX_KEYS = 256;
+constexpr int SHORT_MAX_SLOTS = 3;
+constexpr int SHORT_MAX_STAGES = 8;
+constexpr int SHORT_SMEM_BYTES = 220 * 1024;
+
+struct ShortArgs {
+    void *o;
+    float *lse;
+    int b, sq, sk, h;
+    float scale_log2;  // scale * log2(e)
+    uint32_t *status;
+    uint32_t flags;
+    // the plan (short_plan): key columns N of S (sk rounded up to 32), the
+    // O accumulator's column in a slot, slot width, slots in use, bytes of
+    // one K or V tile (N rows), bytes of one stage (Q + K + V), stages
+    int n_keys, o_off, slot_cols, nslot, kv_bytes, stage_bytes, nstage;
+};
+
+// Fills the plan fields of `a` for sk keys and head dim d; false if the
+// short forward does not take this shape.
+bool short_plan(int sk, int d, ShortArgs *a);
+
+cudaError_t launch_fwd_short(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const ShortArgs &a, int grid,
+                             cudaStream_t stream);
 
 // ------------------------------------------------------------ backward
 struct BwdArgs {
@@ -106,6 +151,7 @@ struct DecodeArgs {
     int page_size = 0;
     int max_pages = 0;
     int num_pages = 0;
+    int box_rows = 0;  // rows of one TMA box: a power of two dividing page_size
     // splits > 1: one arrival counter per (batch, query block, head), zero
     // between calls; the split that arrives last reduces the partials of its
     // rows and sets the counter back to zero. nullptr: the combine kernel
@@ -120,6 +166,7 @@ cudaError_t launch_combine(int d, bool bf16, const float *o_part, const float *l
                            float *lse, int b, int sq, int h, int splits, cudaStream_t stream);
 
 constexpr uint32_t kFlagSkipLoads = 1u;
+constexpr uint32_t kFlagGeneralFwd = 2u;  // test hook: short problems take the general forward
 
 // ------------------------------------------------------------ host helpers (api.cu)
 // None of these allocates device memory.

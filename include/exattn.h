@@ -177,14 +177,15 @@ attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const voi
                                          cudaStream_t stream);
 
 /*
- * Split-KV decode of one new query row per sequence from a paged KV cache.
- * Paged caches are not on the pages beyond a mention ("Why FlashAttention is
- * fast", section 5, item 2: FlashAttention with a paged KV cache is the
- * standard for long contexts); the layout read here is the common one.
- *   q            [b, 1, h, d] (device, 16-byte aligned)
+ * Split-KV decode of new query rows from a paged KV cache. Paged caches are
+ * not on the pages beyond a mention ("Why FlashAttention is fast", section
+ * 5, item 2: FlashAttention with a paged KV cache is the standard for long
+ * contexts); the layout read here is the common one.
+ *   q            [b, sq, h, d] (device, 16-byte aligned): the sq new rows of
+ *                each sequence (the flash-decoding issue's 1 to 10 new tokens)
  *   k_pages,
  *   v_pages      page pools [num_pages, page_size, h, d] (device, 16-byte
- *                aligned); page_size must be a multiple of 256
+ *                aligned); page_size must be a multiple of 16
  *                (ATTN_ERR_UNSUPPORTED otherwise)
  *   block_table  int32 [b, max_pages_per_seq] (device): logical page p of
  *                sequence i is pool page block_table[i * max_pages_per_seq + p]
@@ -192,13 +193,30 @@ attn_status_t attn_decode_splitkv_causal(const void *q, const void *k, const voi
  *                <= max_pages_per_seq * page_size (values outside are
  *                clamped; entries of the table past a sequence's last page
  *                are not used)
- *   o, lse       [b, 1, h, d] and fp32 [b, h, 1]
- * The split count (num_splits = 0: the heuristic) is chosen for the longest
- * allowed sequence, since the lengths are only known on the device; splits
- * past a sequence's end are empty. A sequence with no key gets O = 0 and
+ *   o, lse       [b, sq, h, d] and fp32 [b, h, sq]
+ *   causal       non-zero: the bottom-right-aligned mask of attn_fwd_causal,
+ *                aligned to each sequence's own key count (row r of sequence
+ *                i sees key j only if j <= r + seqlens_k[i] - sq); rows that
+ *                see no key get O = 0 and LSE = -inf
+ * With sq == 1 the splits run on the CUDA-core kernel (pages read in boxes of
+ * at most a page); with sq > 1 on the tensor-core forward kernel, whose
+ * 128-key tiles are gathered from the pages and whose rows past a
+ * sequence's end are zero-filled or zeroed in shared memory, so stale page
+ * data (even NaN) never reaches O. The split count (num_splits = 0: the
+ * heuristic of attn_decode_num_splits) is chosen for the longest allowed
+ * sequence, since the lengths are only known on the device; splits past a
+ * sequence's end are empty. A sequence with no key gets O = 0 and
  * LSE = -inf. The reduce, the workspace and the errors are those of
  * attn_decode_splitkv_ex.
  */
+attn_status_t attn_decode_paged_ex(const void *q, const void *k_pages, const void *v_pages,
+                                   const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                                   float *lse, int b, int sq, int h, int d, int num_pages,
+                                   int page_size, int max_pages_per_seq, float scale,
+                                   int num_splits, int causal, attn_dtype_t dtype,
+                                   cudaStream_t stream);
+
+/* attn_decode_paged_ex with one new row per sequence (sq = 1, q [b, 1, h, d]). */
 attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
                                 const int32_t *block_table, const int32_t *seqlens_k, void *o,
                                 float *lse, int b, int h, int d, int num_pages, int page_size,
@@ -292,12 +310,16 @@ const char *attn_status_string(attn_status_t status);
 void attn_release_workspace(void);
 
 /*
- * Test hook for the bounded waits. ATTN_DEBUG_SKIP_LOADS makes the next
- * launched kernels issue no loads at all, so their first wait runs out and
- * they return with a timeout status instead of hanging. 0 restores normal
- * operation. Host-side only; never needed in production.
+ * Test hooks, host-side only and never needed in production; 0 restores
+ * normal operation. ATTN_DEBUG_SKIP_LOADS makes the next launched kernels
+ * issue no loads at all, so their first wait runs out and they return with
+ * a timeout status instead of hanging. ATTN_DEBUG_GENERAL_FWD makes forward
+ * calls with at most 256 keys and d <= 64, which normally run the short
+ * forward kernel (all keys of a head in one tile), run the general
+ * key-tile-loop kernel instead, so that both can be checked on one shape.
  */
 #define ATTN_DEBUG_SKIP_LOADS 1u
+#define ATTN_DEBUG_GENERAL_FWD 2u
 void attn_debug_set_flags(unsigned int flags);
 
 /* Library ABI version (major * 100 + minor). */

@@ -444,7 +444,54 @@ __global__ void __launch_bounds__(DecGeom<D, ST>::THREADS)
 
     if (warp == G::NCW) {
         // ---------------------------------------------------- producer
-        if (lane == 0 && !(a.flags & kFlagSkipLoads)) {
+        if (PAGED && !(a.flags & kFlagSkipLoads)) {
+            // A paged cache's blocks are gathered as boxes of at most a page
+            // (box_rows, a power of two dividing page_size, so none crosses a
+            // page), one box per lane: the block-table lookups and TMA issues
+            // of a block run side by side (a 64-key block of 16-key pages is
+            // four boxes per tensor). Lane 0 waits for the stage and arms it.
+            // Rows past the sequence's end are masked by the consumers; their
+            // page index is only kept in range.
+            if (lane == 0) {
+                tma_prefetch_desc(&tk);
+                tma_prefetch_desc(&tv);
+            }
+            const uint64_t stream_once = policy_evict_first();
+            const int boxes = G::BN / a.box_rows;  // at most 32
+            int issued = 0;
+            for (int blk = blk0; blk < blk1; ++blk, ++issued) {
+                const int s = issued % G::STAGES;
+                const uint32_t ph = (issued / G::STAGES) & 1;
+                int r = blk * G::BN + lane * a.box_rows;
+                int outer = 0;
+                if (static_cast<int>(lane) < boxes) {
+                    const int lp = min(r / a.page_size, a.max_pages - 1);
+                    const int pg = __ldg(a.block_table + static_cast<int64_t>(batch) * a.max_pages + lp);
+                    outer = min(max(pg, 0), a.num_pages - 1);
+                    r -= lp * a.page_size;
+                }
+                bool got = true;
+                if (lane == 0) {
+                    got = mbar_wait(empty(s), ph ^ 1, g, 1);
+                    if (got) mbar_arrive_expect_tx(full(s), G::STAGE_BYTES);
+                }
+                if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                if (static_cast<int>(lane) < boxes) {
+                    const uint32_t dst = sbase + s * G::STAGE_BYTES + lane * a.box_rows * D * 2;
+                    tma_load_4d_hint(dst, &tk, full(s), 0, head, r, outer, stream_once);
+                    tma_load_4d_hint(dst + G::BLOCK_BYTES, &tv, full(s), 0, head, r, outer,
+                                     stream_once);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                WaitGuard drain = g;
+                uint32_t no_abort = 0;
+                drain.abort = &no_abort;
+                for (int i = (issued > G::STAGES ? issued - G::STAGES : 0); i < issued; ++i)
+                    mbar_wait(full(i % G::STAGES), (i / G::STAGES) & 1, drain, 2);
+            }
+        } else if (!PAGED && lane == 0 && !(a.flags & kFlagSkipLoads)) {
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
             const uint64_t stream_once = policy_evict_first();
@@ -455,26 +502,13 @@ __global__ void __launch_bounds__(DecGeom<D, ST>::THREADS)
                 if (!mbar_wait(empty(s), ph ^ 1, g, 1)) break;
                 mbar_arrive_expect_tx(full(s), G::STAGE_BYTES);
                 const uint32_t dst = sbase + s * G::STAGE_BYTES;
-                // a paged cache's boxes are at most a page high (box_rows, a
-                // power of two dividing page_size), so none crosses a page
-                const int box_rows = PAGED ? a.box_rows : G::BOX_ROWS;
-                const int boxes = PAGED ? G::BN / box_rows : G::BOXES;
-#pragma unroll 4
-                for (int x = 0; x < boxes; ++x) {
-                    int r = blk * G::BN + x * box_rows;
-                    int outer = batch;
-                    if constexpr (PAGED) {
-                        // Rows past the sequence's end are masked by the
-                        // consumers; their page index is only kept in range.
-                        const int lp = min(r / a.page_size, a.max_pages - 1);
-                        const int pg = a.block_table[static_cast<int64_t>(batch) * a.max_pages + lp];
-                        outer = min(max(pg, 0), a.num_pages - 1);
-                        r -= lp * a.page_size;
-                    }
-                    tma_load_4d_hint(dst + x * box_rows * D * 2, &tk, full(s), 0, head, r, outer,
+#pragma unroll
+                for (int x = 0; x < G::BOXES; ++x) {
+                    const int r = blk * G::BN + x * G::BOX_ROWS;
+                    tma_load_4d_hint(dst + x * G::BOX_ROWS * D * 2, &tk, full(s), 0, head, r, batch,
                                      stream_once);
-                    tma_load_4d_hint(dst + G::BLOCK_BYTES + x * box_rows * D * 2, &tv, full(s), 0,
-                                     head, r, outer, stream_once);
+                    tma_load_4d_hint(dst + G::BLOCK_BYTES + x * G::BOX_ROWS * D * 2, &tv, full(s), 0,
+                                     head, r, batch, stream_once);
                 }
             }
             WaitGuard drain = g;

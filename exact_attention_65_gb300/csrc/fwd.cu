@@ -219,33 +219,9 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
             const CUtensorMap *map = (i & 1) ? tv : tk;
             const uint32_t dst = sbase + G::OFF_KV + s * G::KV_TILE_BYTES;
             const int row0 = (x.kv0 + (i >> 1)) * G::BN;
-            if constexpr (PAGED) {
-                // Paged: boxes of box_rows rows, each inside one page (looked
-                // up in the block table). A box wholly past the sequence's end
-                // is addressed past the last pool page, so TMA fills it with
-                // zeros; rows past the end inside the last box hold stale data
-                // (masked for K, zeroed for V before the P V MMA).
-                for (int r = 0; r < G::BN; r += a.box_rows) {
-                    const int key = row0 + r;
-                    int page = a.num_pages, prow = 0;
-                    if (key < x.sk) {
-                        const int lp = key / a.page_size;
-                        page = min(max(__ldg(a.block_table +
-                                             static_cast<int64_t>(x.batch) * a.max_pages + lp),
-                                       0),
-                                   a.num_pages - 1);
-                        prow = key - lp * a.page_size;
-                    }
-                    for (int p = 0; p < G::PANELS; ++p)
-                        tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES + r * G::ROW_BYTES, map,
-                                         bar(G::BAR_KVF + s), p * G::PANEL_ELEMS, x.head, prow,
-                                         page, keep);
-                }
-            } else {
-                for (int p = 0; p < G::PANELS; ++p)
-                    tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES, map, bar(G::BAR_KVF + s),
-                                     p * G::PANEL_ELEMS, x.head, row0, x.batch, keep);
-            }
+            for (int p = 0; p < G::PANELS; ++p)
+                tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES, map, bar(G::BAR_KVF + s),
+                                 p * G::PANEL_ELEMS, x.head, row0, x.batch, keep);
             ++n_issued;
         }
     }
@@ -258,6 +234,91 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
         mbar_wait(bar(G::BAR_QF + n % G::QBUF), (n / G::QBUF) & 1, drain, 9);
     for (int n = (n_issued > G::SLOTS ? n_issued - G::SLOTS : 0); n < n_issued; ++n)
         mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
+}
+
+// The producer for paged caches, run by the whole of warp 0: lane 0 waits
+// for the slots and arms their barriers, and the K/V tiles are gathered as
+// boxes of box_rows rows (each inside one page), one box per lane, so that
+// the block-table lookups and TMA issues of a tile run side by side instead
+// of one after another (a tile of 16-key pages is 8 boxes per panel). A box
+// wholly past the sequence's end is addressed past the last pool page, so
+// TMA fills it with zeros; rows past the end inside the last box hold stale
+// data (masked for K, zeroed for V before the P V MMA).
+template <int D, bool SPLIT, bool PAGED>
+__device__ __forceinline__ void fwd_producer_paged(const CUtensorMap *tq, const CUtensorMap *tk,
+                                                   const CUtensorMap *tv, uint32_t sbase, int nqb,
+                                                   int units, int nkv, const FwdArgs &a,
+                                                   const WaitGuard &g) {
+    using G = FwdGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t keep = nqb > 1 ? policy_evict_last() : policy_evict_first();
+    const int nbox = G::BN / a.box_rows;  // 1 .. 8
+
+    int q_issued = 0, n_issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
+        const int qb = q_issued % G::QBUF;
+        bool got = true;
+        if (lane == 0) {
+            got = mbar_wait(bar(G::BAR_QE + qb), ((q_issued / G::QBUF) & 1) ^ 1, g, 1);
+            if (got) {
+                mbar_arrive_expect_tx(bar(G::BAR_QF + qb), x.n_qt * G::Q_TILE_BYTES);
+                for (int t = 0; t < x.n_qt; ++t)
+                    for (int p = 0; p < G::PANELS; ++p)
+                        tma_load_4d(sbase + G::OFF_Q + qb * G::Q_BUF_BYTES + t * G::Q_TILE_BYTES +
+                                        p * G::Q_PANEL_BYTES,
+                                    tq, bar(G::BAR_QF + qb), p * G::PANEL_ELEMS, x.head,
+                                    x.m0 + t * G::BM, x.batch);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        ++q_issued;
+        for (int i = 0; i < 2 * x.nkv; ++i) {  // K_j at i = 2j, V_j at i = 2j + 1
+            const int s = n_issued % G::SLOTS;
+            const uint32_t ph = (n_issued / G::SLOTS) & 1;
+            // this lane's box: its page is looked up before the slot is waited for
+            const int key = (x.kv0 + (i >> 1)) * G::BN + static_cast<int>(lane) * a.box_rows;
+            int page = a.num_pages, prow = 0;
+            if (static_cast<int>(lane) < nbox && key < x.sk) {
+                const int lp = key / a.page_size;
+                page = min(max(__ldg(a.block_table + static_cast<int64_t>(x.batch) * a.max_pages + lp),
+                               0),
+                           a.num_pages - 1);
+                prow = key - lp * a.page_size;
+            }
+            bool free_slot = true;
+            if (lane == 0) {
+                free_slot = mbar_wait(bar(G::BAR_KVE + s), ph ^ 1, g, 2);
+                if (free_slot) mbar_arrive_expect_tx(bar(G::BAR_KVF + s), G::KV_TILE_BYTES);
+            }
+            if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+                ok = false;
+                break;
+            }
+            if (static_cast<int>(lane) < nbox) {
+                const CUtensorMap *map = (i & 1) ? tv : tk;
+                const uint32_t dst = sbase + G::OFF_KV + s * G::KV_TILE_BYTES +
+                                     lane * a.box_rows * G::ROW_BYTES;
+                for (int p = 0; p < G::PANELS; ++p)
+                    tma_load_4d_hint(dst + p * G::KV_PANEL_BYTES, map, bar(G::BAR_KVF + s),
+                                     p * G::PANEL_ELEMS, x.head, prow, page, keep);
+            }
+            __syncwarp();
+            ++n_issued;
+        }
+    }
+    // Never leave the CTA with a copy still landing in shared memory.
+    if (lane == 0) {
+        WaitGuard drain = g;
+        uint32_t no_abort = 0;
+        drain.abort = &no_abort;
+        for (int n = (q_issued > G::QBUF ? q_issued - G::QBUF : 0); n < q_issued; ++n)
+            mbar_wait(bar(G::BAR_QF + n % G::QBUF), (n / G::QBUF) & 1, drain, 9);
+        for (int n = (n_issued > G::SLOTS ? n_issued - G::SLOTS : 0); n < n_issued; ++n)
+            mbar_wait(bar(G::BAR_KVF + n % G::SLOTS), (n / G::SLOTS) & 1, drain, 10);
+    }
 }
 
 // Paged caches: a unit's last K/V tile can end inside the sequence's last
@@ -746,8 +807,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp < 4) {
         reg_dealloc<kRegsControl>();
         if (warp == 0) {
-            if (lane == 0 && !(a.flags & kFlagSkipLoads))
-                fwd_producer<D, SPLIT, PAGED>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+            if constexpr (PAGED) {
+                if (!(a.flags & kFlagSkipLoads))
+                    fwd_producer_paged<D, SPLIT, PAGED>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+            } else {
+                if (lane == 0 && !(a.flags & kFlagSkipLoads))
+                    fwd_producer<D, SPLIT, PAGED>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
+            }
         } else if (warp == 1) {
             if (lane == 0) fwd_mma<D, BF16, SPLIT, PAGED>(sbase, tmem, nqb, units, nkv, a, g);
         } else if (PAGED && !(a.flags & kFlagSkipLoads)) {

@@ -158,6 +158,16 @@ def test_paged_several_rows_match_contiguous_decode(gpu):
             assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill_many_rows(gpu, oracle_mod, causal):
+    """A chunk of many new rows per sequence from a paged cache (chunked
+    prefill): 700 rows (three 256-row query blocks) over sequences of up to
+    1500 keys in 64-key pages, through the same tensor-core path."""
+    lens = [1500, 1111, 700]
+    q, kp, vp, table, seqlens = _make(3, 4, 128, 64, 24, lens, torch.bfloat16, 109, sq=700)
+    _run(gpu, oracle_mod, q, kp, vp, table, seqlens, 0, causal=causal)
+
+
 def test_paged_rejects_unsupported_page_size(gpu):
     q = torch.zeros((1, 1, 1, 128), dtype=torch.bfloat16, device="cuda")
     kp = torch.zeros((2, 40, 1, 128), dtype=torch.bfloat16, device="cuda")

@@ -271,7 +271,9 @@ def run_ours(args):
 
     def flush():
         flush_buf.zero_()
-        clean_buf.sum()
+        # one reduction kernel reading the whole buffer (int32 max: no
+        # conversion pass, so nothing else is written)
+        clean_buf.view(torch.int32).max()
 
     def flush_write_only():
         flush_buf.zero_()

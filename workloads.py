@@ -81,6 +81,8 @@ WORKLOADS = {
         Workload("decode_b8_h48_sk8192", "decode", 8, 1, 8192, 48, 128, torch.bfloat16),
         Workload("decode_b1_h16_sk32768", "decode", 1, 1, 32768, 16, 128, torch.bfloat16),
         Workload("long_fwd", "fwd", 1, 8192, 8192, 32, 128, torch.bfloat16),
+        # the flash-decoding issue's several new tokens, on the b1 h16 cache
+        Workload("decode_b1_h16_sk32768_sq10", "decode", 1, 10, 32768, 16, 128, torch.bfloat16),
     ]
 }
 

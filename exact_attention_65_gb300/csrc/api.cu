@@ -82,6 +82,9 @@ struct DeviceState {
     int num_sms = 0;
     // copy streams of the host-buffer forward, made on first use
     cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
+    // the backward's second compute stream (its query-tile kernel runs there
+    // beside the key-tile kernel), made on first use
+    cudaStream_t s_side = nullptr;
     // The split decode's workspace, one per stream: arrival counters of the
     // in-kernel reduce (all zero whenever a call starts) and the per-split
     // partials. Calls on one stream are ordered, so each call may reuse them.
@@ -149,6 +152,24 @@ attn_status_t copy_streams(DeviceState *ds) {
         return ATTN_ERR_CUDA;
     }
     return ATTN_OK;
+}
+
+// The backward's side stream (non-blocking, kept for the life of the
+// process); nullptr when `stream` is being captured into a graph or the
+// stream cannot be made, and the tile kernels then run one after the other.
+cudaStream_t side_stream(DeviceState *ds, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!ds->s_side && cudaStreamCreateWithFlags(&ds->s_side, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        ds->s_side = nullptr;
+    }
+    return ds->s_side;
 }
 
 // The split decode's per-stream workspace: at least n zeroed arrival
@@ -676,7 +697,7 @@ static attn_status_t run_bwd(const void *q, const void *k, const void *v, const 
         return ATTN_ERR_NO_MEMORY;
     }
     a.dvec = static_cast<float *>(ws);
-    const cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream);
+    const cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream, side_stream(ds, stream));
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }

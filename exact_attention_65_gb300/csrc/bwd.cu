@@ -672,7 +672,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, int MODE, bool BF16, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
+                         const CUtensorMap &tdo, const BwdArgs &a, int max_ctas,
+                         cudaStream_t stream) {
     using G = BwdGeom<D>;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -686,16 +687,55 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     }
     const int64_t ntiles = MODE == kBwdDQ ? (a.sq + G::BT - 1) / G::BT : (a.sk + G::BT - 1) / G::BT;
     const int64_t units = ntiles * a.h * a.b;
-    const int64_t ctas = units < a.num_sms ? units : a.num_sms;
+    const int64_t ctas = units < max_ctas ? units : max_ctas;
     bwd_kernel<D, MODE, BF16, CAUSAL>
         <<<static_cast<unsigned>(ctas), kBwdThreads, G::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }
 
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_bwd_tiles(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream,
+                             cudaStream_t side) {
+    using G = BwdGeom<D>;
+    if (side == nullptr) {
+        cudaError_t e = launch_bwd_t<D, kBwdDKV, BF16, CAUSAL>(tq, tk, tv, tdo, a, a.num_sms, stream);
+        if (e != cudaSuccess) return e;
+        return launch_bwd_t<D, kBwdDQ, BF16, CAUSAL>(tq, tk, tv, tdo, a, a.num_sms, stream);
+    }
+    // SM shares in proportion to the work: a key-tile step (four products)
+    // costs about 1.1 times a query-tile step (three, two of them reading
+    // their A operand from TMEM)
+    const int64_t u_kv = (a.sk + G::BT - 1) / G::BT * a.h * a.b;
+    const int64_t u_q = (a.sq + G::BT - 1) / G::BT * a.h * a.b;
+    const double w_kv = 1.1 * static_cast<double>(u_kv) * a.sq, w_q = static_cast<double>(u_q) * a.sk;
+    int c_kv = static_cast<int>(a.num_sms * w_kv / (w_kv + w_q) + 0.5);
+    c_kv = c_kv < 1 ? 1 : (c_kv > a.num_sms - 1 ? a.num_sms - 1 : c_kv);
+    int c_q = a.num_sms - c_kv;
+    if (u_kv + u_q <= a.num_sms) {  // every unit has an SM of its own
+        c_kv = static_cast<int>(u_kv);
+        c_q = static_cast<int>(u_q);
+    }
+    cudaEvent_t ev_d = nullptr, ev_q = nullptr;
+    cudaError_t e = cudaEventCreateWithFlags(&ev_d, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_q, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_d, stream);            // D is made
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev_d, 0);
+    if (e == cudaSuccess) e = launch_bwd_t<D, kBwdDKV, BF16, CAUSAL>(tq, tk, tv, tdo, a, c_kv, stream);
+    if (e == cudaSuccess) e = launch_bwd_t<D, kBwdDQ, BF16, CAUSAL>(tq, tk, tv, tdo, a, c_q, side);
+    // join: work queued on `stream` afterwards waits for dQ as well
+    if (e == cudaSuccess) e = cudaEventRecord(ev_q, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev_q, 0);
+    if (ev_d) cudaEventDestroy(ev_d);
+    if (ev_q) cudaEventDestroy(ev_q);
+    return e;
+}
+
 template <int D, bool BF16>
 cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
-    // D = rowsum(dO * O), then dK/dV, then dQ
+                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream,
+                         cudaStream_t side) {
+    // D = rowsum(dO * O), then dK/dV and dQ
     constexpr int RPW = 32 / (D / 8);
     const int64_t rows = static_cast<int64_t>(a.b) * a.sq * a.h;
     const int64_t warps = (rows + RPW - 1) / RPW;
@@ -704,25 +744,19 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
         a.sq, a.h);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (a.causal) {
-        e = launch_bwd_t<D, kBwdDKV, BF16, true>(tq, tk, tv, tdo, a, stream);
-        if (e != cudaSuccess) return e;
-        return launch_bwd_t<D, kBwdDQ, BF16, true>(tq, tk, tv, tdo, a, stream);
-    }
-    e = launch_bwd_t<D, kBwdDKV, BF16, false>(tq, tk, tv, tdo, a, stream);
-    if (e != cudaSuccess) return e;
-    return launch_bwd_t<D, kBwdDQ, BF16, false>(tq, tk, tv, tdo, a, stream);
+    return a.causal ? launch_bwd_tiles<D, BF16, true>(tq, tk, tv, tdo, a, stream, side)
+                    : launch_bwd_tiles<D, BF16, false>(tq, tk, tv, tdo, a, stream, side);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,
-                       cudaStream_t stream) {
-#define EXATTN_BWD_CASE(DD)                                                \
-    case DD:                                                               \
-        return bf16 ? launch_bwd_d<DD, true>(tq, tk, tv, tdo, a, stream)   \
-                    : launch_bwd_d<DD, false>(tq, tk, tv, tdo, a, stream);
+                       cudaStream_t stream, cudaStream_t side) {
+#define EXATTN_BWD_CASE(DD)                                                      \
+    case DD:                                                                     \
+        return bf16 ? launch_bwd_d<DD, true>(tq, tk, tv, tdo, a, stream, side)   \
+                    : launch_bwd_d<DD, false>(tq, tk, tv, tdo, a, stream, side);
     switch (d) {
         EXATTN_BWD_CASE(16)
         EXATTN_BWD_CASE(32)

@@ -110,9 +110,13 @@ struct BwdArgs {
     int causal;  // the forward's bottom-right-aligned causal mask
 };
 
+// D, then the key-tile (dK, dV) and query-tile (dQ) kernels. With a side
+// stream the two tile kernels run at the same time, on SM shares in
+// proportion to their work (they are independent once D is made); without
+// one they run one after the other on `stream`, each on every SM.
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,
-                       cudaStream_t stream);
+                       cudaStream_t stream, cudaStream_t side);
 
 // ------------------------------------------------------------ decode
 // Keys are streamed in blocks of 16 KB per tensor (dec_block_rows(d) rows).

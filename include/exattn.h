@@ -111,6 +111,10 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
  *                    except lse, device pointers, 16-byte aligned.
  * Every output element is written. A workspace of 4 * b * h * sq bytes is
  * taken stream-ordered from the device's default memory pool and returned.
+ * The key-tile (dK, dV) and query-tile (dQ) kernels run at the same time,
+ * the second on a library stream forked from and joined back to `stream` by
+ * events (one after the other on `stream` while it is being captured into a
+ * graph); the call stays stream-ordered on `stream`.
  * Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be had.
  */
 attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,

@@ -79,3 +79,34 @@ def test_bwd_causal_fp16(gpu, oracle_mod, d):
 def test_bwd_causal_many_units_per_cta(gpu, oracle_mod):
     """Causal with more tiles than SMs: units of very different lengths."""
     _check_bwd(gpu, oracle_mod, 4, 640, 640, 48, 64, torch.bfloat16, 101, causal=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_graph_capture_and_user_stream_match_eager(gpu, causal):
+    """The key-tile and query-tile kernels run side by side on the caller's
+    stream and a library stream joined back to it; under graph capture they
+    run one after the other on the captured stream. Both give bit-identical
+    gradients, also when the call is made on a user stream."""
+    b, s, h, d = 2, 700, 8, 128
+    q, k, v = (t.cuda() for t in workloads.make_qkv(b, s, s, h, d, torch.bfloat16, seed=113))
+    do = torch.randn((b, s, h, d), generator=torch.Generator().manual_seed(114)).to(
+        torch.bfloat16).cuda()
+    o, lse = gpu.attn_fwd(q, k, v, causal=causal)
+    ref = gpu.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        got = gpu.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    side.synchronize()
+    for a_, b_ in zip(ref, got):
+        assert torch.equal(a_, b_)
+    outs = [torch.empty_like(t) for t in ref]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu.attn_bwd(q, k, v, o, lse, do, dq=outs[0], dk=outs[1], dv=outs[2], causal=causal)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    for a_, b_ in zip(ref, outs):
+        assert torch.equal(a_, b_)

@@ -252,6 +252,26 @@ attn_status_t alloc_partials(int64_t splits, int b, int sq, int h, int d, cudaSt
     return ATTN_OK;
 }
 
+// Partials of the tensor-core kernel over key ranges: the stream's own
+// workspace (kept per stream: no allocation per call), or, while the stream
+// is being captured into a graph, a workspace of the call's own, returned in
+// *owned for the caller to free after the reduce.
+attn_status_t range_partials(DeviceState *ds, int64_t splits, int b, int sq, int h, int d,
+                             cudaStream_t stream, void **owned, float **o_part, float **lse_part) {
+    const int64_t rows = static_cast<int64_t>(b) * sq * h;
+    const size_t o_bytes = static_cast<size_t>(splits * rows * d) * sizeof(float);
+    const size_t l_bytes = static_cast<size_t>(splits * rows) * sizeof(float);
+    uint32_t *counters = nullptr;
+    void *part = nullptr;
+    *owned = nullptr;
+    if (stream_workspace(ds, stream, 1, o_bytes + l_bytes, &counters, &part)) {
+        *o_part = static_cast<float *>(part);
+        *lse_part = reinterpret_cast<float *>(static_cast<char *>(part) + o_bytes);
+        return ATTN_OK;
+    }
+    return alloc_partials(splits, b, sq, h, d, stream, owned, o_part, lse_part);
+}
+
 // The CUDA-core split decode with splits > 1 (a.o, a.lse, sizes and splits
 // set): the stream's own workspace and the in-kernel reduce, or, while the
 // stream is being captured, a workspace of its own and the reduce kernel.
@@ -287,7 +307,7 @@ attn_status_t run_split_decode(DeviceState *ds, int d, bool bf16, const CUtensor
 // so that no split is empty.
 attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b,
                       int sq, int sk, int h, int d, float scale, bool bf16, int64_t splits,
-                      bool causal, const DeviceState *ds, cudaStream_t stream) {
+                      bool causal, DeviceState *ds, cudaStream_t stream) {
     const int64_t nkv = cdiv(sk, FWD_BN);
     if (splits > nkv) splits = nkv;
     if (splits > DEC_MAX_SPLITS) splits = DEC_MAX_SPLITS;
@@ -362,12 +382,12 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (splits == 1)
         return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     void *ws = nullptr;
-    attn_status_t st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
+    attn_status_t st = range_partials(ds, splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
     if (st != ATTN_OK) return st;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, stream);
     if (e == cudaSuccess)
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    const cudaError_t ef = ws != nullptr ? cudaFreeAsync(ws, stream) : cudaSuccess;
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -381,7 +401,7 @@ attn_status_t run_fwd_paged(const void *q, const void *k_pages, const void *v_pa
                             const int32_t *block_table, const int32_t *seqlens, void *o,
                             float *lse, int b, int sq, int h, int d, int num_pages, int page_size,
                             int max_pages, float scale, int num_splits, bool causal, bool bf16,
-                            const DeviceState *ds, cudaStream_t stream) {
+                            DeviceState *ds, cudaStream_t stream) {
     const int64_t sk_max = static_cast<int64_t>(max_pages) * page_size;
     const int64_t nkv = cdiv(sk_max, FWD_BN);
     int64_t splits =
@@ -430,12 +450,12 @@ attn_status_t run_fwd_paged(const void *q, const void *k_pages, const void *v_pa
     if (splits == 1)
         return launch_fwd(d, bf16, tq, tk, tv, a, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     void *ws = nullptr;
-    attn_status_t st = alloc_partials(splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
+    attn_status_t st = range_partials(ds, splits, b, sq, h, d, stream, &ws, &a.o_part, &a.lse_part);
     if (st != ATTN_OK) return st;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, stream);
     if (e == cudaSuccess)
         e = launch_combine(d, bf16, a.o_part, a.lse_part, o, lse, b, sq, h, a.splits, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    const cudaError_t ef = ws != nullptr ? cudaFreeAsync(ws, stream) : cudaSuccess;
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

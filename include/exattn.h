@@ -145,9 +145,10 @@ attn_status_t attn_bwd_causal(const void *q, const void *k, const void *v, const
  * (batch, head) that finishes last reduces it, found through arrival
  * counters (zero between calls) that the library keeps per stream together
  * with the partials (calls on a stream are ordered, so each reuses them;
- * grown stream-ordered on demand, freed by attn_release_workspace). While
- * the stream is being captured into a graph, and with sq > 1, the partials
- * are taken per call as below and a second kernel reduces instead.
+ * grown stream-ordered on demand, freed by attn_release_workspace). With
+ * sq > 1 the partials come from the same per-stream workspace and a second
+ * kernel reduces them. While the stream is being captured into a graph, the
+ * partials are taken per call as below and the second kernel reduces.
  * num_splits = 0 lets attn_decode_num_splits() choose; a positive value is
  * clamped to the number of key blocks. With one split the first kernel
  * writes O and LSE directly and no workspace is used. Any sq >= 1 is
@@ -156,9 +157,9 @@ attn_status_t attn_bwd_causal(const void *q, const void *k, const void *v, const
  * forward kernel, so each K/V byte is read once for all query rows of a
  * head (the issue's case of 1 to 10 new tokens); its key blocks are tiles of
  * 128 keys and a requested count is lowered so that no split is empty.
- * A per-call workspace is taken stream-ordered from the device's default
- * memory pool and returned after the reduce; it is kept cached in the pool
- * until attn_release_workspace().
+ * Under graph capture the per-call workspace is taken stream-ordered from
+ * the device's default memory pool and returned after the reduce; it is
+ * kept cached in the pool until attn_release_workspace().
  */
 attn_status_t attn_decode_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                                   int b, int sq, int sk, int h, int d, float scale,

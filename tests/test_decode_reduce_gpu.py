@@ -136,3 +136,36 @@ def test_release_then_decode_again(gpu, oracle_mod):
         assert gpu.attn_get_device_status() == gpu.ATTN_OK
         compare(o, lse, *ref)
         gpu.attn_release_workspace()
+
+
+def test_several_rows_share_the_stream_workspace(gpu, oracle_mod):
+    """Several-row decodes (tensor-core kernel, partials in the stream's
+    workspace, reduce kernel) interleaved with one-row decodes (in-kernel
+    reduce) on one stream, with growing and shrinking partials; then the same
+    several-row call captured into a graph (per-call workspace) gives the
+    same bits."""
+    cases = [(1, 1, 5000, 4, 7), (2, 10, 3000, 8, 3), (1, 1, 5000, 4, 9), (1, 16, 9000, 6, 40),
+             (2, 10, 3000, 8, 3), (1, 2, 700, 3, 5)]
+    inputs = {c: workloads.make_qkv(c[0], c[1], c[2], c[3], 128, torch.bfloat16, seed=31 + i)
+              for i, c in enumerate(cases)}
+    refs = {c: oracle_mod.attention(*inputs[c], 1 / math.sqrt(128)) for c in cases}
+    outs = {}
+    for c in cases:
+        o, lse = gpu.attn_decode_splitkv(*(t.cuda() for t in inputs[c]), num_splits=c[4])
+        assert gpu.attn_get_device_status() == gpu.ATTN_OK
+        compare(o, lse, *refs[c])
+        outs[c] = (o, lse)
+    c = cases[1]
+    qd, kd, vd = (t.cuda() for t in inputs[c])
+    o3 = torch.empty_like(outs[c][0])
+    l3 = torch.empty_like(outs[c][1])
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            gpu.attn_decode_splitkv(qd, kd, vd, num_splits=c[4], out=o3, lse=l3)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    assert torch.equal(outs[c][0], o3) and torch.equal(outs[c][1], l3)

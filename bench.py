@@ -453,7 +453,21 @@ def measure_extras(ea, dev, flush, stream, peaks):
                                  "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)}
         del q, k, v
     # backward pass (dQ, dK, dV); FLOP = the five products of the chain
-    # rule, 10*b*h*sq*sk*d (the dQ pass recomputes two of them, not counted)
+    # rule, 10*b*h*sq*sk*d (the dQ pass recomputes two of them, not counted);
+    # the small-head shapes are the ones the flash-attn timing issue times
+    # forward and backward
+    for name in ("small_head_b2_s300", "small_head_b512_s150"):
+        w = workloads.WORKLOADS[name]
+        q, k, v = rand(w)
+        do = torch.randn((w.b, w.sq, w.h, w.d), generator=gen, device=dev).to(w.dtype)
+        o, lse = ea.attn_fwd(q, k, v, scale=w.scale)
+        fn = lambda: ea.attn_bwd(q, k, v, o, lse, do, scale=w.scale)  # noqa: E731
+        (ms,), _ = time_loop([fn], 10, 3, flush, stream)
+        tf = 10 * w.b * w.h * w.sq * w.sk * w.d / (ms * 1e-3) / 1e12
+        io = 8 * w.b * w.sq * w.h * w.d * w.elem_bytes  # q, k, v, o, dO read; dq, dk, dv written
+        out[f"{name}/backward"] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 2),
+                                   "GB/s": round(io / (ms * 1e-3) / 1e9, 1)}
+        del q, k, v, do, o, lse
     for name in ("mid_fwd", "long_fwd"):
         w = workloads.WORKLOADS[name]
         q, k, v = rand(w)

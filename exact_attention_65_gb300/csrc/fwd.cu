@@ -93,6 +93,14 @@ struct FwdGeom {
     static constexpr int BAR_VLAND = BAR_DONE + 1;  // paged: last V tile landed (MMA -> zeroing)
     static constexpr int BAR_VFIX = BAR_VLAND + 1;  // paged: its stale rows zeroed (zeroing -> MMA)
     static constexpr int NUM_BARS = BAR_VFIX + 1;
+    // The kernel for units with one live query tile puts S of odd key tiles
+    // in the second tile's S columns and uses that tile's barriers, idle
+    // there: its S full and P full barriers, and its O full barrier for one
+    // completed by every P V (an O rescale waits for the one before it).
+    static constexpr int BAR_SF2 = BAR_SF + 1;
+    static constexpr int BAR_PF2 = BAR_PF + 1;
+    static constexpr int BAR_PVD = BAR_OF + 1;
+    static_assert(QT == 2, "the one-tile kernel borrows the second tile's barriers");
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int USED = OFF_MISC + 16;
     // Keep one CTA per SM: it owns all 512 TMEM columns.
@@ -373,7 +381,7 @@ __device__ __forceinline__ void fwd_fix_v(uint32_t sbase, int nqb, int units, in
     }
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED>
+template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
 __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, int units,
                                         int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
@@ -394,11 +402,93 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     int p_cnt[G::QT] = {};  // P phases consumed per query tile
     int o_cnt[G::QT] = {};  // units finished per query tile
     int fix_cnt = 0;        // paged V tiles handed over by the zeroing warps
+    int p2_cnt = 0;         // P phases of odd key tiles in one-tile units
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++it_u) {
         const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
         const int qbuf = it_u % G::QBUF;
         if (!mbar_wait(bar(G::BAR_QF + qbuf), (it_u / G::QBUF) & 1, g, 4)) break;
+        if constexpr (ONE) {
+            // One live query tile: S of key tile j goes to the S columns of
+            // tile (j & 1), so S_{j+1} is made while the softmax works on
+            // S_j, and O (tile 0's) accumulates P_j V_j from either. S_{j+2}
+            // is issued right after P_j V_j, which has read the columns it
+            // overwrites (the tensor core runs a thread's MMAs in order).
+            const uint32_t tO = tmem + G::TMEM_O_OFF;
+            auto issue_s = [&](int j) {
+                const int nk = 2 * (kv_base + j), ks = nk % G::SLOTS;
+                if (!mbar_wait(bar(G::BAR_KVF + ks), (nk / G::SLOTS) & 1, g, 5)) return false;
+                tc_fence_after();
+                const uint32_t tS = tmem + (j & 1) * G::TMEM_TILE_STRIDE;
+                const uint64_t qdesc = dq + ((qbuf * G::Q_BUF_BYTES) >> 4);
+                const uint64_t kdesc = dk + ((ks * G::KV_TILE_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int p = (kk * 16) / G::PANEL_ELEMS;
+                    const int off = ((kk * 16) % G::PANEL_ELEMS) * 2;
+                    mma_ss(tS, qdesc + ((p * G::Q_PANEL_BYTES + off) >> 4),
+                           kdesc + ((p * G::KV_PANEL_BYTES + off) >> 4), idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar((j & 1) ? G::BAR_SF2 : G::BAR_SF));
+                mma_commit(bar(G::BAR_KVE + ks));                           // last read of K_j
+                if (j == x.nkv - 1) mma_commit(bar(G::BAR_QE + qbuf));     // ... and of this Q
+                return true;
+            };
+            if (x.nkv > 0) ok = issue_s(0);
+            if (ok && x.nkv > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < x.nkv; ++j) {
+                const int nv = 2 * (kv_base + j) + 1, vs = nv % G::SLOTS;
+                if (!mbar_wait(bar(G::BAR_KVF + vs), (nv / G::SLOTS) & 1, g, 6)) {
+                    ok = false;
+                    break;
+                }
+                if (j == x.nkv - 1 && unit_needs_v_fix<PAGED>(x)) {
+                    // a paged unit's last V tile has landed; wait for its
+                    // stale rows to be zeroed
+                    mbar_arrive(bar(G::BAR_VLAND));
+                    if (!mbar_wait(bar(G::BAR_VFIX), fix_cnt & 1, g, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    ++fix_cnt;
+                }
+                // the first P V overwrites O: the previous unit's epilogue
+                // must have read it out
+                if (j == 0 && !mbar_wait(bar(G::BAR_OE), (o_cnt[0] & 1) ^ 1, g, 7)) {
+                    ok = false;
+                    break;
+                }
+                const bool odd = j & 1;
+                if (!mbar_wait(bar(odd ? G::BAR_PF2 : G::BAR_PF), (odd ? p2_cnt : p_cnt[0]) & 1, g,
+                               8)) {
+                    ok = false;
+                    break;
+                }
+                if (odd)
+                    ++p2_cnt;
+                else
+                    ++p_cnt[0];
+                tc_fence_after();
+                const uint32_t tP = tmem + (j & 1) * G::TMEM_TILE_STRIDE;
+                const uint64_t vdesc = dv + ((vs * G::KV_TILE_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < G::BN / 16; ++kk)
+                    mma_ts(tO, tP + kk * 8, vdesc + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(G::BAR_KVE + vs));  // last read of V_j
+                mma_commit(bar(G::BAR_PVD));
+                if (j == x.nkv - 1) mma_commit(bar(G::BAR_OF));
+                if (j + 2 < x.nkv) ok = issue_s(j + 2);
+            }
+            if (!ok) break;
+            if (x.nkv == 0) {  // causal: a unit that sees no key
+                mma_commit(bar(G::BAR_QE + qbuf));
+                mma_commit(bar(G::BAR_OF));
+            }
+            kv_base += x.nkv;
+            ++o_cnt[0];
+            continue;
+        }
         // The issue order keeps the tensor core's short instruction queue fed:
         // every barrier wait or commit sits right after a group of MMAs, while
         // those are still queued, never in a clump between two groups.
@@ -490,7 +580,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED>
+template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
 __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4, int nqb,
                                             int units, int nkv, const FwdArgs &a,
                                             const WaitGuard &g) {
@@ -498,15 +588,19 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     const uint32_t lane = threadIdx.x & 31;
     const int row = q4 * 32 + lane;
-    const uint32_t tS = tmem + t * G::TMEM_TILE_STRIDE + (static_cast<uint32_t>(q4 * 32) << 16);
-    const uint32_t tO = tS + G::TMEM_O_OFF;
+    const uint32_t tS0 = tmem + t * G::TMEM_TILE_STRIDE + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t tO = tS0 + G::TMEM_O_OFF;
     const float c = a.scale_log2;
     const bool c_pos = c >= 0.f;
     int s_cnt = 0, o_cnt = 0;
+    // one-tile units (tile 0's warpgroup only): S phases of odd key tiles,
+    // and P V products issued so far
+    int s2_cnt = 0, pv_done = 0;
 
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit x = unit_of<SPLIT, PAGED>(u, nqb, nkv, a);
         if (t >= x.n_qt) continue;
+        constexpr bool single = ONE;
         const int tile_row0 = x.m0 + t * G::BM;
         const int grow = tile_row0 + row;
         // A warp whose 32 rows all lie past sq skips the math but keeps the
@@ -517,8 +611,16 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         float l = 0.f;            // running sum of 2^(s*c - m_ref)
         bool alive = true;
         for (int j = 0; j < x.nkv; ++j) {
-            const bool ok = mbar_wait(bar(G::BAR_SF + t), s_cnt & 1, g, 13);
-            ++s_cnt;
+            // S_j: in one-tile units odd key tiles use the second tile's S
+            // columns and barriers
+            const bool alt = single && (j & 1);
+            const uint32_t tS = alt ? tS0 + G::TMEM_TILE_STRIDE : tS0;
+            const bool ok = mbar_wait(bar(alt ? G::BAR_SF2 : G::BAR_SF + t),
+                                      (alt ? s2_cnt : s_cnt) & 1, g, 13);
+            if (alt)
+                ++s2_cnt;
+            else
+                ++s_cnt;
             if (!__all_sync(0xffffffffu, ok)) {
                 alive = false;
                 break;
@@ -650,8 +752,20 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                     tmem_st32(tS + half * (G::BN / 4), pk);
                 }
                 if (rescale) {
-                    // O row *= alpha; P_{j-1} V_{j-1} has completed (S_j's commit
-                    // covers it). 16 columns at a time keeps this path spill-free.
+                    // O row *= alpha once P_{j-1} V_{j-1} has completed: S_j's
+                    // commit covers it where S_j was issued after it; a one-tile
+                    // unit issues S_j earlier and waits for that P V's own
+                    // barrier (at most one phase ahead of this wait: the next
+                    // P V needs this P_j). 16 columns at a time keeps this path
+                    // spill-free.
+                    if (single) {
+                        const bool okv = mbar_wait(bar(G::BAR_PVD), (pv_done + j - 1) & 1, g, 15);
+                        if (!__all_sync(0xffffffffu, okv)) {
+                            alive = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 16) {
                         uint32_t ov[16];
@@ -666,7 +780,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
+                if (lane == 0) mbar_arrive(bar(alt ? G::BAR_PF2 : G::BAR_PF + t));
                 float a0, a1, a2, a3;
                 f2_split(acc2[0], a0, a1);
                 f2_split(acc2[1], a2, a3);
@@ -674,10 +788,11 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
             } else {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(G::BAR_PF + t));
+                if (lane == 0) mbar_arrive(bar(alt ? G::BAR_PF2 : G::BAR_PF + t));
             }
         }
         if (!alive) return;
+        if (single) pv_done += x.nkv;
 
         // ---------------------------------------------------- epilogue
         const bool ok = mbar_wait(bar(G::BAR_OF + t), o_cnt & 1, g, 14);
@@ -756,7 +871,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     }
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED>
+template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -815,14 +930,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                     fwd_producer<D, SPLIT, PAGED>(&tq, &tk, &tv, sbase, nqb, units, nkv, a, g);
             }
         } else if (warp == 1) {
-            if (lane == 0) fwd_mma<D, BF16, SPLIT, PAGED>(sbase, tmem, nqb, units, nkv, a, g);
+            if (lane == 0) fwd_mma<D, BF16, SPLIT, PAGED, ONE>(sbase, tmem, nqb, units, nkv, a, g);
         } else if (PAGED && !(a.flags & kFlagSkipLoads)) {
             fwd_fix_v<D, SPLIT, PAGED>(sbase, nqb, units, nkv, a, g);
         }
     } else {
         reg_alloc<kRegsSoftmax>();
-        fwd_softmax<D, BF16, SPLIT, PAGED>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units, nkv,
-                                           a, g);
+        fwd_softmax<D, BF16, SPLIT, PAGED, ONE>(sbase, tmem, (warp - 4) >> 2, warp & 3, nqb, units,
+                                                nkv, a, g);
     }
 
     tc_fence_before();
@@ -831,7 +946,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED>
+template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
     using G = FwdGeom<D>;
@@ -840,7 +955,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_kernel<D, BF16, SPLIT, PAGED>,
+        e = cudaFuncSetAttribute(fwd_kernel<D, BF16, SPLIT, PAGED, ONE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -855,9 +970,24 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     const int64_t waves = (units + a.num_sms - 1) / a.num_sms;
     const int64_t ctas =
         a.causal ? (units < a.num_sms ? units : a.num_sms) : (units + waves - 1) / waves;
-    fwd_kernel<D, BF16, SPLIT, PAGED>
+    fwd_kernel<D, BF16, SPLIT, PAGED, ONE>
         <<<static_cast<unsigned>(ctas), FWD_THREADS, G::SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
+}
+
+// At most 128 query rows against more than one key tile: every unit has one
+// live query tile, and the kernel compiled for that case (double-buffered S)
+// runs (b1 h16 sk32768 with 10 rows: 55.6 -> 49.7 us; b8 h48 sk8192: 285 ->
+// 241 us). With a single key tile there is nothing to overlap (b64 s100 h16:
+// 32.8 -> 33.9 us), so the two-tile kernel keeps those. The two paths are
+// separate kernels: compiled into one, the two-tile calls lost about 6 us
+// per launch (b4 s512 h32: 26.6 -> 32.8 us) though they never ran the other.
+template <int D, bool BF16, bool SPLIT, bool PAGED>
+cudaError_t launch_fwd_o(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const FwdArgs &a, cudaStream_t stream) {
+    return a.sq <= FWD_BM && a.sk > FWD_BN
+               ? launch_fwd_t<D, BF16, SPLIT, PAGED, true>(tq, tk, tv, a, stream)
+               : launch_fwd_t<D, BF16, SPLIT, PAGED, false>(tq, tk, tv, a, stream);
 }
 
 template <int D, bool BF16>
@@ -865,9 +995,9 @@ cudaError_t launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
                          const FwdArgs &a, cudaStream_t stream) {
     // three instantiations: the plain forward, key ranges / causal, and key
     // ranges over a paged cache; each keeps only the code it needs
-    if (a.block_table) return launch_fwd_t<D, BF16, true, true>(tq, tk, tv, a, stream);
-    return (a.splits > 1 || a.causal) ? launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, stream)
-                                      : launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, stream);
+    if (a.block_table) return launch_fwd_o<D, BF16, true, true>(tq, tk, tv, a, stream);
+    return (a.splits > 1 || a.causal) ? launch_fwd_o<D, BF16, true, false>(tq, tk, tv, a, stream)
+                                      : launch_fwd_o<D, BF16, false, false>(tq, tk, tv, a, stream);
 }
 
 }  // namespace

@@ -20,10 +20,14 @@ def _inputs(sq, sk):
     return [t.cuda() for t in workloads.make_qkv(1, sq, sk, 2, 128, torch.bfloat16, seed=37)]
 
 
-@pytest.mark.parametrize("which", ["fwd", "decode"])
+@pytest.mark.parametrize("which", ["fwd", "fwd_two_tiles", "decode", "decode_rows"])
 def test_skipped_loads_time_out_and_recover(gpu, which):
-    q, k, v = _inputs(1 if which == "decode" else 64, 256)
-    call = (lambda: gpu.attn_fwd(q, k, v)) if which == "fwd" else (
+    # fwd: 64 rows (the one-tile forward kernel); fwd_two_tiles: 300 rows
+    # (the two-tile kernel); decode: one row (the CUDA-core split kernel);
+    # decode_rows: 10 rows (the one-tile forward kernel on key ranges)
+    sq = {"fwd": 64, "fwd_two_tiles": 300, "decode": 1, "decode_rows": 10}[which]
+    q, k, v = _inputs(sq, 256)
+    call = (lambda: gpu.attn_fwd(q, k, v)) if which.startswith("fwd") else (
         lambda: gpu.attn_decode_splitkv(q, k, v, num_splits=2))
     assert gpu.attn_get_device_status() == gpu.ATTN_OK
     gpu.attn_debug_set_flags(gpu.ATTN_DEBUG_SKIP_LOADS)
@@ -37,7 +41,7 @@ def test_skipped_loads_time_out_and_recover(gpu, which):
     assert status == gpu.ATTN_ERR_DEVICE_TIMEOUT
     assert elapsed < 60
     kernel = gpu.attn_last_timeout_site() >> 8
-    assert kernel == (1 if which == "fwd" else 2)
+    assert kernel == (2 if which == "decode" else 1)
     # the status word was cleared and the context still works
     assert gpu.attn_get_device_status() == gpu.ATTN_OK
     o, lse = call()

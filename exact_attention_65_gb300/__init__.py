@@ -31,6 +31,7 @@ ATTN_ERR_NO_MEMORY = 4
 ATTN_ERR_DEVICE_TIMEOUT = 5
 ATTN_DEBUG_SKIP_LOADS = 1
 ATTN_DEBUG_GENERAL_FWD = 2
+ATTN_DEBUG_GENERAL_BWD = 4
 
 _lock = threading.Lock()
 _lib = None

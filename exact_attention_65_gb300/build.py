@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libexattn.so")
 
-SOURCES = ["api.cu", "fwd.cu", "fwd_short.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_short.cu", "bwd.cu", "bwd_short.cu", "decode.cu",
+           "decode_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "ptx.cuh"),
            os.path.join(INCLUDE, "exattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -498,7 +498,7 @@ const char *attn_status_string(attn_status_t s) {
 }
 
 void attn_debug_set_flags(unsigned int flags) {
-    g_flags = flags & (ATTN_DEBUG_SKIP_LOADS | ATTN_DEBUG_GENERAL_FWD);
+    g_flags = flags & (ATTN_DEBUG_SKIP_LOADS | ATTN_DEBUG_GENERAL_FWD | ATTN_DEBUG_GENERAL_BWD);
 }
 
 unsigned int attn_last_timeout_site(void) { return g_last_site; }
@@ -685,12 +685,18 @@ static attn_status_t run_bwd(const void *q, const void *k, const void *v, const 
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     const bool bf16 = dtype == ATTN_BF16;
+    // short problems: one kernel finishes each (batch, head); its Q / dO boxes
+    // hold every query row (one or two 128-row tiles), its K / V boxes every key
+    const bool short_bwd =
+        !(debug_flags() & kFlagGeneralBwd) && bwd_short_plan(sq, sk, d, causal);
     const int box0 = fwd_row_bytes(d) / 2;
+    const int qrows = short_bwd ? static_cast<int>(cdiv(sq, 128) * 128) : 128;
+    const int krows = short_bwd ? static_cast<int>(cdiv(sk, 32) * 32) : 128;
     CUtensorMap tq, tk, tv, tdo;
-    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, 128, fwd_swizzle(d)) ||
-        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, 128, fwd_swizzle(d)) ||
-        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, 128, fwd_swizzle(d)) ||
-        !encode_4d(&tdo, dout, bf16, d, h, sq, b, box0, 128, fwd_swizzle(d)))
+    if (!encode_4d(&tq, q, bf16, d, h, sq, b, box0, qrows, fwd_swizzle(d)) ||
+        !encode_4d(&tk, k, bf16, d, h, sk, b, box0, krows, fwd_swizzle(d)) ||
+        !encode_4d(&tv, v, bf16, d, h, sk, b, box0, krows, fwd_swizzle(d)) ||
+        !encode_4d(&tdo, dout, bf16, d, h, sq, b, box0, qrows, fwd_swizzle(d)))
         return ATTN_ERR_CUDA;
     BwdArgs a;
     a.o = o;
@@ -717,7 +723,9 @@ static attn_status_t run_bwd(const void *q, const void *k, const void *v, const 
         return ATTN_ERR_NO_MEMORY;
     }
     a.dvec = static_cast<float *>(ws);
-    const cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream, side_stream(ds, stream));
+    const cudaError_t e = short_bwd
+                              ? launch_bwd_short(d, bf16, tq, tk, tv, tdo, a, stream)
+                              : launch_bwd(d, bf16, tq, tk, tv, tdo, a, stream, side_stream(ds, stream));
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -731,24 +731,41 @@ cudaError_t launch_bwd_tiles(const CUtensorMap &tq, const CUtensorMap &tk, const
     return e;
 }
 
+// D = rowsum(dO * O), fp32 [b, h, sq]
 template <int D, bool BF16>
-cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream,
-                         cudaStream_t side) {
-    // D = rowsum(dO * O), then dK/dV and dQ
+cudaError_t launch_dot_d(const BwdArgs &a, cudaStream_t stream) {
     constexpr int RPW = 32 / (D / 8);
     const int64_t rows = static_cast<int64_t>(a.b) * a.sq * a.h;
     const int64_t warps = (rows + RPW - 1) / RPW;
     bwd_dot_kernel<D, BF16><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
         static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.dvec, a.b,
         a.sq, a.h);
-    cudaError_t e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream,
+                         cudaStream_t side) {
+    // D, then dK/dV and dQ
+    cudaError_t e = launch_dot_d<D, BF16>(a, stream);
     if (e != cudaSuccess) return e;
     return a.causal ? launch_bwd_tiles<D, BF16, true>(tq, tk, tv, tdo, a, stream, side)
                     : launch_bwd_tiles<D, BF16, false>(tq, tk, tv, tdo, a, stream, side);
 }
 
 }  // namespace
+
+cudaError_t launch_bwd_dot(int d, bool bf16, const BwdArgs &a, cudaStream_t stream) {
+    switch (d) {
+        case 16: return bf16 ? launch_dot_d<16, true>(a, stream) : launch_dot_d<16, false>(a, stream);
+        case 32: return bf16 ? launch_dot_d<32, true>(a, stream) : launch_dot_d<32, false>(a, stream);
+        case 64: return bf16 ? launch_dot_d<64, true>(a, stream) : launch_dot_d<64, false>(a, stream);
+        case 128:
+            return bf16 ? launch_dot_d<128, true>(a, stream) : launch_dot_d<128, false>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,

@@ -110,6 +110,21 @@ struct BwdArgs {
     int causal;  // the forward's bottom-right-aligned causal mask
 };
 
+// Backward for short sequences (bwd_short.cu): one (batch, head) per work
+// item, all of its keys in one row of S, dQ, dK and dV finished in the CTA.
+// Head dims 16 and 32, at most 256 query rows, and keys while TMEM holds S,
+// dP, dQ, dK and dV (sk <= 192 at d = 16, <= 160 at d = 32); not causal.
+constexpr int SBWD_MAX_Q = 256;   // query rows (two 128-row tiles)
+constexpr int SBWD_MAX_K = 256;   // key rows a K / V box can hold
+bool bwd_short_plan(int sq, int sk, int d, bool causal);
+// D = rowsum(dO * O) into a.dvec (the first kernel of every backward).
+cudaError_t launch_bwd_dot(int d, bool bf16, const BwdArgs &a, cudaStream_t stream);
+// The short backward proper; Q and dO maps with boxes of 128 * ceil(sq /
+// 128) rows, K and V maps with boxes of sk rounded up to 32 rows.
+cudaError_t launch_bwd_short(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const CUtensorMap &tdo, const BwdArgs &a,
+                             cudaStream_t stream);
+
 // D, then the key-tile (dK, dV) and query-tile (dQ) kernels. With a side
 // stream the two tile kernels run at the same time, on SM shares in
 // proportion to their work (they are independent once D is made); without
@@ -171,6 +186,7 @@ cudaError_t launch_combine(int d, bool bf16, const float *o_part, const float *l
 
 constexpr uint32_t kFlagSkipLoads = 1u;
 constexpr uint32_t kFlagGeneralFwd = 2u;  // test hook: short problems take the general forward
+constexpr uint32_t kFlagGeneralBwd = 4u;  // test hook: short problems take the tile backward
 
 // ------------------------------------------------------------ host helpers (api.cu)
 // None of these allocates device memory.

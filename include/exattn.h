@@ -114,7 +114,9 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
  * The key-tile (dK, dV) and query-tile (dQ) kernels run at the same time,
  * the second on a library stream forked from and joined back to `stream` by
  * events (one after the other on `stream` while it is being captured into a
- * graph); the call stays stream-ordered on `stream`.
+ * graph); the call stays stream-ordered on `stream`. Short problems (d 16
+ * or 32, sq <= 256, sk <= 160) run one kernel instead, which finishes each
+ * (batch, head) in one CTA (all of its keys in one row of S).
  * Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be had.
  */
 attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
@@ -322,9 +324,12 @@ void attn_release_workspace(void);
  * calls with at most 256 keys and d <= 64, which normally run the short
  * forward kernel (all keys of a head in one tile), run the general
  * key-tile-loop kernel instead, so that both can be checked on one shape.
+ * ATTN_DEBUG_GENERAL_BWD does the same for the short backward kernel: those
+ * backward calls run the key-tile and query-tile kernels.
  */
 #define ATTN_DEBUG_SKIP_LOADS 1u
 #define ATTN_DEBUG_GENERAL_FWD 2u
+#define ATTN_DEBUG_GENERAL_BWD 4u
 void attn_debug_set_flags(unsigned int flags);
 
 /* Library ABI version (major * 100 + minor). */

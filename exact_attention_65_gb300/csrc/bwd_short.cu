@@ -27,6 +27,9 @@
 //   warp 0        TMA producer: Q, dO, K, V of an item into a stage (two
 //                 stages at d = 16, one at d = 32).
 //   warp 1        TMEM owner and MMA issuer (one thread).
+//   warp 2        stages each item's LSE and D rows in shared memory ahead
+//                 of its use (the elementwise warps would otherwise start
+//                 each item with a global load of them).
 //   warps 4-11    elementwise: group g (warps 4 + 4g .. 7 + 4g) holds all
 //                 128 lanes and takes the 16-key chunks c with c % 2 == g;
 //                 group g also writes dK and dV of key M tile g.
@@ -61,7 +64,9 @@ struct SbGeom {
     static constexpr int STAGES = D == 16 ? 2 : 1;
     static constexpr int OFF_P = STAGES * STAGE_BYTES;
     static constexpr int OFF_DS = OFF_P + SB_PDS_BYTES;
-    static constexpr int OFF_BAR = OFF_DS + SB_PDS_BYTES;
+    // per stage: the item's LSE (log2 units) and D, SBWD_MAX_Q floats each
+    static constexpr int OFF_LD = OFF_DS + SB_PDS_BYTES;
+    static constexpr int OFF_BAR = OFF_LD + STAGES * 2 * SBWD_MAX_Q * 4;
     static constexpr int BAR_INF = 0;              // [2] an item's inputs landed
     static constexpr int BAR_INE = BAR_INF + 2;    // [2] its last MMA has read them
     static constexpr int BAR_SF = BAR_INE + 2;     // a tile's S and dP in TMEM
@@ -71,7 +76,8 @@ struct SbGeom {
     static constexpr int BAR_QE = BAR_QF + 1;      // dQ read out (8 warps)
     static constexpr int BAR_KVF = BAR_QE + 1;     // the item's dK and dV in TMEM
     static constexpr int BAR_KVE = BAR_KVF + 1;    // read out (8 warps)
-    static constexpr int BAR_DONE = BAR_KVE + 1;
+    static constexpr int BAR_LDF = BAR_KVE + 1;    // [2] an item's LSE and D staged (warp 2)
+    static constexpr int BAR_DONE = BAR_LDF + 2;
     static constexpr int NUM_BARS = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -134,6 +140,34 @@ __device__ __forceinline__ void sb_producer(const CUtensorMap *tq, const CUtenso
     drain.abort = &no_abort;
     for (int m = (n > G::STAGES ? n - G::STAGES : 0); m < n; ++m)
         mbar_wait(bar(G::BAR_INF + m % G::STAGES), (m / G::STAGES) & 1, drain, 41);
+}
+
+// Warp 2: LSE * log2(e) and D of every query row of the CTA's items into the
+// item's stage, as soon as the stage's previous item is done with it (rows
+// past sq get LSE = +inf, hence P = 0, and D = 0).
+template <int D>
+__device__ __forceinline__ void sb_stage_ld(uint8_t *smem, uint32_t sbase, int items,
+                                            const BwdArgs &a, const WaitGuard &g) {
+    using G = SbGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    constexpr float kLog2e = 1.4426950408889634f;
+    const uint32_t lane = threadIdx.x & 31;
+    const int rows = (a.sq + SB_QT - 1) / SB_QT * SB_QT;
+    int n = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+        const int st = n % G::STAGES;
+        const bool ok = mbar_wait(bar(G::BAR_INE + st), ((n / G::STAGES) & 1) ^ 1, g, 51);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        const int64_t base = static_cast<int64_t>(it) * a.sq;  // (batch, head) = it
+        float *ld = reinterpret_cast<float *>(smem + G::OFF_LD) + st * 2 * SBWD_MAX_Q;
+        for (int r = lane; r < rows; r += 32) {
+            const bool v = r < a.sq;
+            ld[r] = v ? a.lse[base + r] * kLog2e : INFINITY;
+            ld[SBWD_MAX_Q + r] = v ? a.dvec[base + r] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(G::BAR_LDF + st));
+    }
 }
 
 // dQ = dS K over STEPS steps of 16 keys, one straight-line run of MMAs: A is
@@ -302,7 +336,6 @@ __device__ __forceinline__ void sb_elementwise(uint8_t *smem, uint32_t sbase, ui
     const int row = q4 * 32 + lane;  // TMEM lane: a query row of the tile (a key row for dK, dV)
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
     const float c = a.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
     const int nch16 = p.n / 16;  // 16-key chunks (even: n is a multiple of 32)
     // this thread's rows of the P and dS panels (row of 128 bytes, 16-byte
     // chunks XOR-swizzled by the row's low three bits)
@@ -313,13 +346,16 @@ __device__ __forceinline__ void sb_elementwise(uint8_t *smem, uint32_t sbase, ui
     for (int i = 0; i < n_items; ++i) {
         const int it = blockIdx.x + i * gridDim.x;
         const int head = it % a.h, batch = it / a.h;
-        const int64_t bh = static_cast<int64_t>(batch) * a.h + head;
+        const int st = i % G::STAGES;
+        const bool okl = mbar_wait(bar(G::BAR_LDF + st), (i / G::STAGES) & 1, g, 52);
+        if (!__all_sync(0xffffffffu, okl)) return;
+        const float *ld = reinterpret_cast<const float *>(smem + G::OFF_LD) + st * 2 * SBWD_MAX_Q;
         for (int qt = 0; qt < p.nqt; ++qt, ++n_tile) {
             const int grow = qt * SB_QT + row;
             const bool valid = grow < a.sq;
             // rows past sq: LSE = +inf makes P = 0, and dO (TMA zero fill) dP = 0
-            const float lse2 = valid ? a.lse[bh * a.sq + grow] * kLog2e : INFINITY;
-            const float drow = valid ? a.dvec[bh * a.sq + grow] : 0.f;
+            const float lse2 = ld[grow];
+            const float drow = ld[SBWD_MAX_Q + grow];
             const bool oks = mbar_wait(bar(G::BAR_SF), n_tile & 1, g, 47);
             if (!__all_sync(0xffffffffu, oks)) return;
             // the previous tile's dV / dK MMAs have read the P and dS panels
@@ -448,6 +484,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i) {
             const bool by_warps = i == G::BAR_PF || i == G::BAR_QE || i == G::BAR_KVE;
+            // BAR_LDF: one arrive by warp 2's lane 0
             mbar_init(bar(i), by_warps ? static_cast<uint32_t>(SB_EW_WARPS) : 1u);
         }
         *abort_flag = 0u;
@@ -474,6 +511,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             sb_producer<D>(&tq, &tk, &tv, &tdo, sbase, items, p, a, g);
     } else if (warp == 1) {
         if (lane == 0) sb_mma<D, BF16>(sbase, tmem, n_items, p, a.sq, g);
+    } else if (warp == 2) {
+        sb_stage_ld<D>(smem, sbase, items, a, g);
     } else if (warp >= 4) {
         sb_elementwise<D, BF16>(smem, sbase, tmem, warp & 3, (warp - 4) >> 2, n_items, p, a, g);
     }

@@ -686,9 +686,14 @@ static attn_status_t run_bwd(const void *q, const void *k, const void *v, const 
     if ((st = device_state(&ds)) != ATTN_OK) return st;
     const bool bf16 = dtype == ATTN_BF16;
     // short problems: one kernel finishes each (batch, head); its Q / dO boxes
-    // hold every query row (one or two 128-row tiles), its K / V boxes every key
-    const bool short_bwd =
-        !(debug_flags() & kFlagGeneralBwd) && bwd_short_plan(sq, sk, d, causal);
+    // hold every query row (one or two 128-row tiles), its K / V boxes every
+    // key. With fewer (batch, head) items than half the SMs it leaves most of
+    // them idle, and the tile kernels, which spread one problem over several
+    // CTAs, win unless the problem is a single tile on each side (b2 s150 h16
+    // d16: 19.5 against 15.7 us; b2 s50: 13.7 against 15.0 us).
+    const bool short_bwd = !(debug_flags() & kFlagGeneralBwd) &&
+                           bwd_short_plan(sq, sk, d, causal) &&
+                           (static_cast<int64_t>(b) * h * 2 >= ds->num_sms || (sq <= 128 && sk <= 128));
     const int box0 = fwd_row_bytes(d) / 2;
     const int qrows = short_bwd ? static_cast<int>(cdiv(sq, 128) * 128) : 128;
     const int krows = short_bwd ? static_cast<int>(cdiv(sk, 32) * 32) : 128;

@@ -115,7 +115,8 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
  * the second on a library stream forked from and joined back to `stream` by
  * events (one after the other on `stream` while it is being captured into a
  * graph); the call stays stream-ordered on `stream`. Short problems (d 16
- * or 32, sq <= 256, sk <= 160) run one kernel instead, which finishes each
+ * or 32, sq <= 256, sk <= 160, not causal, with b * h at least half the SM
+ * count or sq, sk <= 128) run one kernel instead, which finishes each
  * (batch, head) in one CTA (all of its keys in one row of S).
  * Errors as attn_fwd; ATTN_ERR_NO_MEMORY if the workspace cannot be had.
  */

@@ -5,9 +5,11 @@ the C ABI. attn_bwd takes it for those shapes; the debug flag
 ATTN_DEBUG_GENERAL_BWD sends the same calls to the key-tile and query-tile
 kernels, which must agree with the oracle too.
 
-Shapes: key counts on both sides of every 32-key chunk edge and of the
-128-key M tile (1, 5, 31, 32, 33, 64, 100, 128, 129, 150, 160), query counts
-from one row to two ragged 128-row tiles (1, 2, 127, 128, 129, 200, 256),
+Shapes (80 (batch, head) items, or one tile on each side, so that the short
+kernel is the one that runs): key counts on both sides of every 16- and
+32-key chunk edge and of the 128-key M tile (1, 5, 31, 32, 33, 64, 100, 128,
+129, 150, 160), query counts from one row to two ragged 128-row tiles (1, 2,
+127, 128, 129, 200, 256),
 both head dims and dtypes, the flash-attn timing issue's small-head shapes
 (b2 s50 and, with fewer batches, s150 at h16 d16), far more items than SMs,
 large scores, and a timeout that the context survives.
@@ -24,6 +26,11 @@ import workloads
 from parity import to_np64
 
 pytestmark = pytest.mark.gpu
+
+# attn_bwd takes the short kernel for these shapes when there are at least
+# half as many (batch, head) items as SMs (or one tile on each side): 40
+# batches of 2 heads are 80 items, past half of this part's 152 SMs
+ITEMS_B = 40
 
 
 def _grads(ea, q, k, v, do, scale, general=False):
@@ -62,18 +69,18 @@ def _check(ea, oracle_mod, b, sq, sk, h, d, dtype, seed, q_mul=1.0, general=Fals
 @pytest.mark.parametrize("d", [16, 32])
 def test_key_counts_and_head_dims(gpu, oracle_mod, sk, d):
     dtype = torch.float16 if d == 16 else torch.bfloat16
-    _check(gpu, oracle_mod, 2, 150, sk, 2, d, dtype, seed=401 + sk)
+    _check(gpu, oracle_mod, ITEMS_B, 150, sk, 2, d, dtype, seed=401 + sk)
 
 
 @pytest.mark.parametrize("sq", [1, 2, 127, 128, 129, 200, 256])
 def test_query_counts(gpu, oracle_mod, sq):
-    _check(gpu, oracle_mod, 2, sq, 150, 2, 16, torch.float16, seed=421 + sq)
+    _check(gpu, oracle_mod, ITEMS_B, sq, 150, 2, 16, torch.float16, seed=421 + sq)
 
 
 @pytest.mark.parametrize("d", [16, 32])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_dtypes(gpu, oracle_mod, d, dtype):
-    _check(gpu, oracle_mod, 1, 140, 120, 3, d, dtype, seed=431 + d)
+    _check(gpu, oracle_mod, ITEMS_B, 140, 120, 2, d, dtype, seed=431 + d)
 
 
 @pytest.mark.parametrize("b,s", [(2, 50), (64, 150)])
@@ -91,12 +98,12 @@ def test_timing_issue_shapes_both_kernels(gpu, oracle_mod, b, s):
 def test_large_scores(gpu, oracle_mod):
     """Scores spread over tens of units: P is exp(S - LSE) with the
     forward's LSE, so nothing overflows however far apart the scores are."""
-    _check(gpu, oracle_mod, 1, 130, 150, 2, 32, torch.bfloat16, seed=451, q_mul=6.0)
+    _check(gpu, oracle_mod, ITEMS_B, 130, 150, 2, 32, torch.bfloat16, seed=451, q_mul=6.0)
 
 
 def test_repeat_calls_are_deterministic(gpu):
-    q, k, v = (t.cuda() for t in workloads.make_qkv(4, 150, 150, 8, 16, torch.float16, seed=461))
-    do = torch.randn((4, 150, 8, 16), generator=torch.Generator().manual_seed(462)).to(
+    q, k, v = (t.cuda() for t in workloads.make_qkv(10, 150, 150, 8, 16, torch.float16, seed=461))
+    do = torch.randn((10, 150, 8, 16), generator=torch.Generator().manual_seed(462)).to(
         torch.float16).cuda()
     o, lse = gpu.attn_fwd(q, k, v)
     a1 = gpu.attn_bwd(q, k, v, o, lse, do)

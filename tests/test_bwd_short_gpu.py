@@ -113,6 +113,33 @@ def test_repeat_calls_are_deterministic(gpu):
         assert torch.equal(x, y)
 
 
+def test_graph_capture_and_user_stream_match_eager(gpu):
+    """The short kernel (and the D = rowsum(dO * O) kernel before it) on a
+    user stream and inside a captured graph give bit-identical gradients."""
+    q, k, v = (t.cuda() for t in workloads.make_qkv(10, 150, 150, 8, 16, torch.float16, seed=481))
+    do = torch.randn((10, 150, 8, 16), generator=torch.Generator().manual_seed(482)).to(
+        torch.float16).cuda()
+    o, lse = gpu.attn_fwd(q, k, v)
+    ref = gpu.attn_bwd(q, k, v, o, lse, do)
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        got = gpu.attn_bwd(q, k, v, o, lse, do)
+    side.synchronize()
+    for a_, b_ in zip(ref, got):
+        assert torch.equal(a_, b_)
+    outs = [torch.empty_like(t) for t in ref]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu.attn_bwd(q, k, v, o, lse, do, dq=outs[0], dk=outs[1], dv=outs[2])
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gpu.attn_get_device_status() == gpu.ATTN_OK
+    for a_, b_ in zip(ref, outs):
+        assert torch.equal(a_, b_)
+
+
 def test_timeout_and_recovery(gpu):
     """ATTN_DEBUG_SKIP_LOADS: the producer issues nothing, the MMA issuer's
     wait for the first item's inputs runs out after its bound, the kernel

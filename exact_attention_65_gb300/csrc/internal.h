@@ -113,7 +113,7 @@ struct BwdArgs {
 // Backward for short sequences (bwd_short.cu): one (batch, head) per work
 // item, all of its keys in one row of S, dQ, dK and dV finished in the CTA.
 // Head dims 16 and 32, at most 256 query rows, and keys while TMEM holds S,
-// dP, dQ, dK and dV (sk <= 192 at d = 16, <= 160 at d = 32); not causal.
+// dP, dQ, dK and dV (sk <= 160); not causal.
 constexpr int SBWD_MAX_Q = 256;   // query rows (two 128-row tiles)
 constexpr int SBWD_MAX_K = 256;   // key rows a K / V box can hold
 bool bwd_short_plan(int sq, int sk, int d, bool causal);

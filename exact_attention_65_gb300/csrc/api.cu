@@ -321,29 +321,44 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     CUtensorMap tq, tk, tv;
     // Short key sequences with small heads (every key of a head in one tile,
     // several tiles in flight per SM): the short forward.
+    // Grouped items (head dim 16, heads in fours) once there are more
+    // one-head tiles than SMs: with fewer, each tile has an SM to itself and
+    // the grouped item's extra step (the block-diagonal copy, four QK^T MMAs)
+    // only lengthens the one chain per SM (b2 s50 h16: 10.2 against 8.2 us).
     ShortArgs sa;
-    if (splits == 1 && !causal && !(debug_flags() & kFlagGeneralFwd) && short_plan(sk, d, &sa)) {
-        const int64_t items = cdiv(sq, SHORT_BM) * h * b;
-        if (items > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-        if (!encode_4d(&tq, q, bf16, d, h, sq, b, d, SHORT_BM, fwd_swizzle(d)) ||
-            !encode_4d(&tk, k, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d)) ||
-            !encode_4d(&tv, v, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d)))
-            return ATTN_ERR_CUDA;
+    const bool grouped_ok = cdiv(sq, SHORT_BM) * h * b > ds->num_sms;
+    if (splits == 1 && !causal && !(debug_flags() & kFlagGeneralFwd) &&
+        short_plan(sq, sk, h, d, grouped_ok, &sa)) {
+        sa.sq = sq;
+        const int64_t su = short_units(sa, b, h);
+        // the CTA-local item counts (grouped: pairs times query blocks) fit an int
+        if (su * (sa.grouped ? sa.nblk : 1) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+        // grouped items read four heads at a time: the same memory viewed as
+        // [b, s, h / 4, 64], 128-byte rows (one 32-row query block per box)
+        const bool ok =
+            sa.grouped
+                ? encode_4d(&tq, q, bf16, 64, h / 4, sq, b, 64, 32, fwd_swizzle(64)) &&
+                      encode_4d(&tk, k, bf16, 64, h / 4, sk, b, 64, sa.n_keys, fwd_swizzle(64)) &&
+                      encode_4d(&tv, v, bf16, 64, h / 4, sk, b, 64, sa.n_keys, fwd_swizzle(64))
+                : encode_4d(&tq, q, bf16, d, h, sq, b, d, SHORT_BM, fwd_swizzle(d)) &&
+                      encode_4d(&tk, k, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d)) &&
+                      encode_4d(&tv, v, bf16, d, h, sk, b, d, sa.n_keys, fwd_swizzle(d));
+        if (!ok) return ATTN_ERR_CUDA;
         sa.o = o;
         sa.lse = lse;
         sa.b = b;
-        sa.sq = sq;
         sa.sk = sk;
         sa.h = h;
         sa.scale_log2 = scale * kLog2e;
         sa.status = ds->status;
         sa.flags = debug_flags();
-        // CTA c takes items c, c + grid, c + 2 grid, ...; a grid that shares
+        // CTA c takes units c, c + grid, c + 2 grid, ...; a grid that shares
         // no factor with the tiles per head deals every CTA each tile index
         // in turn (with 2 tiles per head and 152 CTAs, half of the CTAs would
-        // get only full first tiles and the other half only short last ones)
-        const int64_t ntile = cdiv(sq, SHORT_BM);
-        int64_t grid = items < ds->num_sms ? items : ds->num_sms;
+        // get only full first tiles and the other half only short last ones;
+        // grouped units are all alike)
+        const int64_t ntile = sa.grouped ? 1 : cdiv(sq, SHORT_BM);
+        int64_t grid = su < ds->num_sms ? su : ds->num_sms;
         auto gcd = [](int64_t x, int64_t y) {
             while (y) {
                 const int64_t t = x % y;
@@ -352,7 +367,7 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
             }
             return x;
         };
-        while (grid > 1 && items > grid && gcd(grid, ntile) != 1) --grid;
+        while (grid > 1 && su > grid && gcd(grid, ntile) != 1) --grid;
         return launch_fwd_short(d, bf16, tq, tk, tv, sa, static_cast<int>(grid), stream) ==
                        cudaSuccess
                    ? ATTN_OK

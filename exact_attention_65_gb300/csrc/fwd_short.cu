@@ -15,10 +15,12 @@
 // TMEM slots, so several items are in flight per SM and the latency chain of each
 // (loads, QK^T, softmax, PV, store) overlaps the others':
 //   warp 0        TMA producer: Q tile, K and V of the item into a ring of
-//                 shared-memory stages.
-//   warp 1        TMEM owner and MMA issuer (one thread): S = Q K^T into the
-//                 item's slot, later O = P V into the same slot.
-//   warps 2-3     idle.
+//                 shared-memory stages (packed items: idle).
+//   warp 1        TMEM owner; issues every QK^T MMA (one thread): S = Q K^T
+//                 into the item's slot.
+//   warp 2        grouped items: copies each query block onto its
+//                 block-diagonal tile; else idle.
+//   warp 3        issues every P V MMA (one thread).
 //   warps 4..     one softmax warpgroup per slot (the kernel is compiled
 //                 for 2 and 3 slots); warpgroup g owns slot g, and thread i
 //                 of warp w owns row 32 (w % 4) + i of its tile.
@@ -30,6 +32,28 @@
 // of chunks whose max exceeds it by more than 8 (log2 units) moves it and
 // rescales the P already stored (rare). So no thread holds a whole score
 // row and each chunk costs one TMEM round trip.
+//
+// Grouped items (head dim 16, heads a multiple of 4). At head dim 16 a
+// query or key row of one head is 32 bytes, with the other heads' rows
+// between them, and loading a head by itself moves 32-byte pieces: a TMA box
+// (or cp.async) of such rows ran at about 7 bytes per cycle per SM, which
+// is what set the pace of whole calls. So four consecutive heads are loaded
+// as one: their rows are 128 contiguous bytes (the [b, s, h / 4, 64] view
+// of the same memory), one TMA box per tile. A work item is one 32-row
+// query block of such a group of four heads, 128 rows in all, and the
+// group's K and V tiles (N keys by 4 x 16) are loaded once and serve every
+// query block of the group. The four heads must not see each other's keys,
+// and one MMA multiplies one A tile by one B tile, so warp 2 copies the
+// query block onto the block diagonal of a zeroed 128 x 64 tile: rows
+// [32p, 32p + 32) hold head p's 16 query columns at columns [16p, 16p + 16)
+// and zeros elsewhere. Four MMAs accumulate S, the p-th over the 16 columns
+// of head p in both the diagonal tile and the group's K tile; every other
+// head's columns are zero in row block p, so each row gets the scores
+// against its own head's keys. P V runs once with N = 64 over the group's V
+// tile (the four heads side by side), and row block p keeps O columns
+// [16p, 16p + 16). A K that holds an infinity or a NaN therefore also turns
+// the other heads of its group to NaN (zero times infinity); the inputs are
+// taken to be finite.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,11 +64,12 @@ namespace exattn {
 namespace {
 
 constexpr int SH_WG = SHORT_MAX_SLOTS;          // most softmax warpgroups
-constexpr int SH_MAX_CHUNKS = SHORT_MAX_KEYS / 32;
 constexpr int SH_BAR_BYTES = 1024;             // barriers and flags, before the tiles
 
 // barriers: full[stages] | empty[stages] | s_full[slots] | p_full[slots] |
-//           o_full[slots] | free[slots] | done
+//           o_full[slots] | free[slots] | done[2] | (grouped items:) diagonal
+//           tile full[stages] | group K/V full[kv stages] | empty[kv stages]
+constexpr int SH_MAX_KV_STAGES = 3;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = BAR_FULL + SHORT_MAX_STAGES;
 constexpr int BAR_SF = BAR_EMPTY + SHORT_MAX_STAGES;
@@ -52,7 +77,11 @@ constexpr int BAR_PF = BAR_SF + SH_WG;
 constexpr int BAR_OF = BAR_PF + SH_WG;
 constexpr int BAR_FREE = BAR_OF + SH_WG;
 constexpr int BAR_DONE = BAR_FREE + SH_WG;
-constexpr int NUM_BARS = BAR_DONE + 1;
+constexpr int BAR_DONE2 = BAR_DONE + 1;
+constexpr int BAR_DF = BAR_DONE2 + 1;
+constexpr int BAR_KVF = BAR_DF + SHORT_MAX_STAGES;
+constexpr int BAR_KVE = BAR_KVF + SH_MAX_KV_STAGES;
+constexpr int NUM_BARS = BAR_KVE + SH_MAX_KV_STAGES;
 constexpr int OFF_MISC = NUM_BARS * 8;
 static_assert(OFF_MISC + 16 <= SH_BAR_BYTES, "barrier area");
 
@@ -84,6 +113,23 @@ __device__ __forceinline__ Item item_of(int it, int ntile, int h) {
     const int r = it / ntile;
     x.head = r % h;
     x.batch = r / h;
+    return x;
+}
+
+// Grouped items: a CTA takes the (batch, group of four heads) pairs c,
+// c + grid, c + 2 grid, ... and runs every 32-row query block of each pair
+// in turn, so its n-th item is block n % nblk of its (n / nblk)-th pair.
+struct GroupItem {
+    int batch, group, blk, k;  // k: the pair's index among this CTA's pairs
+};
+
+__device__ __forceinline__ GroupItem group_item(int n, int nblk, int hg) {
+    GroupItem x;
+    x.k = n / nblk;
+    x.blk = n - x.k * nblk;
+    const int pair = static_cast<int>(blockIdx.x) + x.k * static_cast<int>(gridDim.x);
+    x.batch = pair / hg;
+    x.group = pair - x.batch * hg;
     return x;
 }
 
@@ -159,6 +205,8 @@ __device__ __forceinline__ void rescale_p(uint32_t tS, int cols, float alpha) {
     }
 }
 
+// Plain items, run by lane 0 of warp 0: each item's Q tile, K and V (three
+// TMA boxes) into one stage, in that order.
 template <int D>
 __device__ __forceinline__ void short_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                                const CUtensorMap *tv, uint32_t sbase,
@@ -175,8 +223,8 @@ __device__ __forceinline__ void short_producer(const CUtensorMap *tq, const CUte
         mbar_arrive_expect_tx(bar(BAR_FULL + st), bytes);
         const uint32_t dst = tiles + st * a.stage_bytes;
         tma_load_4d(dst, tq, bar(BAR_FULL + st), 0, x.head, x.tile * SHORT_BM, x.batch);
-        tma_load_4d(dst + G::Q_BYTES, tk, bar(BAR_FULL + st), 0, x.head, 0, x.batch);
-        tma_load_4d(dst + G::Q_BYTES + a.kv_bytes, tv, bar(BAR_FULL + st), 0, x.head, 0, x.batch);
+        tma_load_4d(dst + a.q_bytes, tk, bar(BAR_FULL + st), 0, x.head, 0, x.batch);
+        tma_load_4d(dst + a.q_bytes + a.kv_bytes, tv, bar(BAR_FULL + st), 0, x.head, 0, x.batch);
     }
     // Never leave the CTA with a copy still landing in shared memory.
     WaitGuard drain = g;
@@ -186,87 +234,214 @@ __device__ __forceinline__ void short_producer(const CUtensorMap *tq, const CUte
         mbar_wait(bar(BAR_FULL + m % a.nstage), (m / a.nstage) & 1, drain, 21);
 }
 
-template <int D, bool BF16>
-__device__ __forceinline__ void short_mma(uint32_t sbase, uint32_t tiles, uint32_t tmem,
-                                          int n_items, const ShortArgs &a, const WaitGuard &g) {
-    using G = ShortGeom<D>;
+// Grouped items, run by lane 0 of warp 0: per pair, the group's K and V
+// tiles (n_keys rows of 128 bytes each) into a ring of kv stages; per item,
+// its 32-row query block of the group (128-byte rows) into the stage's
+// staging area. The next pair's K/V is requested after its first query
+// block, once a kv stage has come free (with three kv stages that is the
+// pair before last, long done).
+// Stage layout (grouped): staging block (32 x 128 bytes), then the
+// block-diagonal query tile (128 x 128 bytes); the kv ring follows the
+// stages: K tile, then V tile, per kv stage.
+__device__ __forceinline__ void group_producer(const CUtensorMap *tq, const CUtensorMap *tk,
+                                               const CUtensorMap *tv, uint32_t sbase,
+                                               uint32_t tiles, int n_items, int hg,
+                                               const ShortArgs &a, const WaitGuard &g) {
     auto bar = [&](int i) { return sbase + 8u * i; };
-    const uint32_t idesc_s = mma_idesc_f16(SHORT_BM, a.n_keys, BF16, false, false);
-    constexpr uint32_t idesc_o = mma_idesc_f16(SHORT_BM, D, BF16, false, true);
-    const uint64_t dk = smem_desc(tiles, 16, G::SBO, G::LAYOUT);  // Q and K, K-major
-    // V, MN-major; d spans one swizzle atom, so the leading offset is not
-    // stepped through (it is set to the tile size, like a panel stride)
-    const uint64_t dv = smem_desc(tiles, a.kv_bytes, G::SBO, G::LAYOUT);
-    const int kv_steps = a.n_keys / 16;
-    // Two queues in item order: QK^T for the next item whose stage has landed
-    // and whose slot the epilogue of the item nslot back has handed back, and
-    // P V for the oldest item whose P is stored. Polled without blocking, so
-    // neither queue waits behind the other's barrier; the wait is bounded
-    // like every other (no progress for the bound, or a CTA-wide abort).
-    int s_next = 0, p_next = 0;
-    uint64_t t0 = global_timer_ns();
-    uint32_t polls = 0;
-    while (p_next < n_items) {
-        bool progressed = false;
-        if (s_next < n_items && s_next - p_next < a.nslot) {
-            const int sl = s_next % a.nslot, st = s_next % a.nstage;
-            if (mbar_test_wait(bar(BAR_FULL + st), (s_next / a.nstage) & 1) &&
-                (s_next < a.nslot ||
-                 mbar_test_wait(bar(BAR_FREE + sl), ((s_next / a.nslot) - 1) & 1))) {
-                tc_fence_after();
-                const uint32_t tS = tmem + sl * a.slot_cols;
-                const uint64_t qd = dk + ((st * a.stage_bytes) >> 4);
-                const uint64_t kd = qd + (G::Q_BYTES >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tS, qd + kk * 2, kd + kk * 2, idesc_s, kk > 0 ? 1u : 0u);
-                mma_commit(bar(BAR_SF + sl));
-                ++s_next;
-                progressed = true;
-            }
-        }
-        if (p_next < s_next) {
-            const int sl = p_next % a.nslot, st = p_next % a.nstage;
-            if (mbar_test_wait(bar(BAR_PF + sl), (p_next / a.nslot) & 1)) {
-                tc_fence_after();
-                const uint32_t tS = tmem + sl * a.slot_cols;
-                const uint64_t vd = dv + ((st * a.stage_bytes + G::Q_BYTES + a.kv_bytes) >> 4);
-                for (int kk = 0; kk < kv_steps; ++kk)
-                    mma_ts(tS + a.o_off, tS + kk * 8, vd + ((kk * 16 * G::ROW_BYTES) >> 4), idesc_o,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(bar(BAR_OF + sl));
-                mma_commit(bar(BAR_EMPTY + st));
-                ++p_next;
-                progressed = true;
-            }
-        }
-        if (progressed) {
-            t0 = global_timer_ns();
-            polls = 0;
-        } else if ((++polls & 15u) == 0u) {
-            if (*g.abort) break;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs || polls >= kWaitMaxPolls) {
-                *g.abort = 1u;
-                atomicCAS(g.status, 0u, (g.kernel << 8) | 22u);
-                break;
-            }
-        }
+    const uint32_t kv_base = tiles + a.nstage * a.stage_bytes;
+    const int npairs = n_items / a.nblk;
+    int kv_n = 0;  // pairs whose K/V have been requested
+    auto load_kv = [&](int k) {
+        const int ks = k % a.nkv_stage;
+        if (!mbar_wait(bar(BAR_KVE + ks), ((k / a.nkv_stage) & 1) ^ 1, g, 28)) return false;
+        const int pair = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        const int bb = pair / hg, gg = pair - (pair / hg) * hg;
+        const uint32_t dst = kv_base + ks * a.kv_stage_bytes;
+        mbar_arrive_expect_tx(bar(BAR_KVF + ks), 2u * a.kv_bytes);
+        tma_load_4d(dst, tk, bar(BAR_KVF + ks), 0, gg, 0, bb);
+        tma_load_4d(dst + a.kv_bytes, tv, bar(BAR_KVF + ks), 0, gg, 0, bb);
+        ++kv_n;
+        return true;
+    };
+    int n = 0;
+    bool ok = npairs > 0 ? load_kv(0) : true;
+    for (; ok && n < n_items; ++n) {
+        const GroupItem x = group_item(n, a.nblk, hg);
+        const int st = n % a.nstage;
+        if (!mbar_wait(bar(BAR_EMPTY + st), ((n / a.nstage) & 1) ^ 1, g, 20)) break;
+        mbar_arrive_expect_tx(bar(BAR_FULL + st), 32u * 128u);
+        tma_load_4d(tiles + st * a.stage_bytes, tq, bar(BAR_FULL + st), 0, x.group, 32 * x.blk,
+                    x.batch);
+        if (x.blk == 0 && x.k + 1 < npairs) ok = load_kv(x.k + 1);
     }
-    // No MMA may still be running when TMEM is released.
-    mma_commit(bar(BAR_DONE));
+    // Never leave the CTA with a copy still landing in shared memory.
     WaitGuard drain = g;
     uint32_t no_abort = 0;
     drain.abort = &no_abort;
-    mbar_wait(bar(BAR_DONE), 0, drain, 25);
+    for (int m = (n > a.nstage ? n - a.nstage : 0); m < n; ++m)
+        mbar_wait(bar(BAR_FULL + m % a.nstage), (m / a.nstage) & 1, drain, 21);
+    for (int k = (kv_n > a.nkv_stage ? kv_n - a.nkv_stage : 0); k < kv_n; ++k)
+        mbar_wait(bar(BAR_KVF + k % a.nkv_stage), (k / a.nkv_stage) & 1, drain, 29);
 }
 
-template <int D, bool BF16>
+// Grouped items, run by warp 2: once an item's staging block has landed,
+// copy head p's 32 bytes of each of its 32 rows to rows [32p, 32p + 32),
+// columns [16p, 16p + 16) of the stage's block-diagonal tile (16 bytes per
+// copy, eight copies per thread: one row each), whose other entries stay
+// zero; then a cross-proxy fence and one arrival per thread on the tile's
+// barrier. Both tiles use the 128-byte swizzle, in which the
+// 16-byte chunk c of row r sits at chunk c ^ (r % 8), and the tile's row
+// 32p + r has the same r % 8 as the staging row r.
+__device__ __forceinline__ void group_copier(uint32_t sbase, uint32_t tiles, int n_items,
+                                             const ShortArgs &a, const WaitGuard &g) {
+    auto bar = [&](int i) { return sbase + 8u * i; };
+    const uint32_t r = threadIdx.x - 64u;  // 0 .. 31: the row of the block
+    for (int n = 0; n < n_items; ++n) {
+        const int st = n % a.nstage;
+        const bool ok = mbar_wait(bar(BAR_FULL + st), (n / a.nstage) & 1, g, 23);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        const uint32_t stg = tiles + st * a.stage_bytes;
+        const uint32_t diag = stg + 32u * 128u;
+#pragma unroll
+        for (uint32_t c = 0; c < 8; ++c) {  // chunk c: head c / 2
+            const uint32_t p = c >> 1;
+            const uint32_t chunk = (c ^ (r & 7u)) << 4;
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(stg + r * 128u + chunk));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             diag + (32u * p + r) * 128u + chunk),
+                         "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(BAR_DF + st));
+    }
+}
+
+// The MMAs are issued by two threads, each waiting (bounded) on its own
+// barriers only: lane 0 of warp 1 issues every QK^T, lane 0 of warp 3 every
+// P V. A single thread polling both queues fell behind once every softmax
+// warp of an item was busy: it shares its SM sub-partition with three
+// softmax warps, and a P V went out up to ~3500 cycles after its P was
+// stored. The two streams need no ordering between them beyond the slot
+// barriers: QK^T of an item waits for the slot's previous epilogue, which
+// follows that item's P V (o_full), and P V waits for P, which follows S.
+template <int D, bool GRP>
+struct MmaGeom {
+    using G = ShortGeom<D>;
+    static constexpr uint32_t SBO = GRP ? 1024u : G::SBO;  // 8 rows of 128 bytes when grouped
+    static constexpr uint32_t LAYOUT = GRP ? kLayoutSw128 : G::LAYOUT;
+    static constexpr uint32_t V_ROW = GRP ? 128u : G::ROW_BYTES;
+};
+
+// Waits until every MMA this thread issued has completed (TMEM is released
+// after both issuers have done so).
+__device__ __forceinline__ void drain_mmas(uint32_t done_bar, const WaitGuard &g, uint32_t site) {
+    mma_commit(done_bar);
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(done_bar, 0, drain, site);
+}
+
+template <int D, bool BF16, bool GRP>
+__device__ __forceinline__ void short_mma_s(uint32_t sbase, uint32_t tiles, uint32_t tmem,
+                                            int n_items, const ShortArgs &a,
+                                            const WaitGuard &g) {
+    using M = MmaGeom<D, GRP>;
+    auto bar = [&](int i) { return sbase + 8u * i; };
+    const uint32_t idesc_s = mma_idesc_f16(SHORT_BM, a.n_keys, BF16, false, false);
+    const uint64_t dk = smem_desc(tiles, 16, M::SBO, M::LAYOUT);  // Q and K, K-major
+    const uint32_t kv_base = a.nstage * a.stage_bytes;  // grouped: the kv ring, after the stages
+    for (int n = 0; n < n_items; ++n) {
+        const int sl = n % a.nslot, st = n % a.nstage;
+        int ks = 0;
+        if constexpr (GRP) {
+            // the block-diagonal tile is made; the first block of a pair
+            // also waits for the pair's K/V (later blocks follow it)
+            const int k = n / a.nblk;
+            ks = k % a.nkv_stage;
+            if (!mbar_wait(bar(BAR_DF + st), (n / a.nstage) & 1, g, 22)) break;
+            if (n == k * a.nblk && !mbar_wait(bar(BAR_KVF + ks), (k / a.nkv_stage) & 1, g, 22))
+                break;
+        } else {
+            if (!mbar_wait(bar(BAR_FULL + st), (n / a.nstage) & 1, g, 22)) break;
+        }
+        if (n >= a.nslot && !mbar_wait(bar(BAR_FREE + sl), ((n / a.nslot) - 1) & 1, g, 22)) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + sl * a.slot_cols;
+        if constexpr (GRP) {
+            static_assert(D == 16, "grouped items: one K = 16 step per head");
+            // the p-th MMA takes head p's 16 columns (32 bytes into the
+            // 128-byte rows) of the diagonal tile and of K
+            const uint64_t qd = dk + ((st * a.stage_bytes + 32u * 128u) >> 4);
+            const uint64_t kd = dk + ((kv_base + ks * a.kv_stage_bytes) >> 4);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) mma_ss(tS, qd + p * 2, kd + p * 2, idesc_s, p > 0 ? 1u : 0u);
+            mma_commit(bar(BAR_SF + sl));
+            mma_commit(bar(BAR_EMPTY + st));  // the stage is read once QK^T is done
+        } else {
+            const uint64_t qd = dk + ((st * a.stage_bytes) >> 4);
+            const uint64_t kd = qd + (a.q_bytes >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tS, qd + kk * 2, kd + kk * 2, idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit(bar(BAR_SF + sl));
+        }
+    }
+    drain_mmas(bar(BAR_DONE), g, 25);
+}
+
+template <int D, bool BF16, bool GRP>
+__device__ __forceinline__ void short_mma_o(uint32_t sbase, uint32_t tiles, uint32_t tmem,
+                                            int n_items, const ShortArgs &a,
+                                            const WaitGuard &g) {
+    using M = MmaGeom<D, GRP>;
+    auto bar = [&](int i) { return sbase + 8u * i; };
+    // grouped items: P V over the group's four heads side by side, N = 64
+    constexpr uint32_t idesc_o = mma_idesc_f16(SHORT_BM, GRP ? 64 : D, BF16, false, true);
+    // V, MN-major; its N columns span one swizzle atom, so the leading offset
+    // is not stepped through (it is set to the tile size, like a panel stride)
+    const uint64_t dv = smem_desc(tiles, a.kv_bytes, M::SBO, M::LAYOUT);
+    const uint32_t kv_base = a.nstage * a.stage_bytes;
+    const int kv_steps = a.n_keys / 16;
+    for (int n = 0; n < n_items; ++n) {
+        const int sl = n % a.nslot, st = n % a.nstage;
+        if (!mbar_wait(bar(BAR_PF + sl), (n / a.nslot) & 1, g, 24)) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + sl * a.slot_cols;
+        int k = 0, ks = 0;
+        uint32_t voff;
+        if constexpr (GRP) {
+            k = n / a.nblk;
+            ks = k % a.nkv_stage;
+            voff = kv_base + ks * a.kv_stage_bytes + a.kv_bytes;
+        } else {
+            voff = st * a.stage_bytes + a.q_bytes + a.kv_bytes;
+        }
+        const uint64_t vd = dv + (voff >> 4);
+        for (int kk = 0; kk < kv_steps; ++kk)
+            mma_ts(tS + a.o_off, tS + kk * 8, vd + ((kk * 16 * M::V_ROW) >> 4), idesc_o,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(bar(BAR_OF + sl));
+        if constexpr (GRP) {
+            // the pair's last block releases its K/V
+            if (n - k * a.nblk == a.nblk - 1) mma_commit(bar(BAR_KVE + ks));
+        } else {
+            mma_commit(bar(BAR_EMPTY + st));
+        }
+    }
+    drain_mmas(bar(BAR_DONE2), g, 26);
+}
+
+template <int D, bool BF16, bool GRP>
 __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int sl, int q4,
                                               int n_items, int ntile, const ShortArgs &a,
                                               const WaitGuard &g) {
     auto bar = [&](int i) { return sbase + 8u * i; };
     const uint32_t lane = threadIdx.x & 31;
-    const int row = q4 * 32 + lane;
     const uint32_t tS = tmem + sl * a.slot_cols + (static_cast<uint32_t>(q4 * 32) << 16);
     const uint32_t tO = tS + a.o_off;
     const float c = a.scale_log2;
@@ -278,9 +453,26 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
 
     int k = 0;
     for (int i = sl; i < n_items; i += a.nslot, ++k) {
-        const Item x = item_of(blockIdx.x + i * gridDim.x, ntile, a.h);
-        const int grow = x.tile * SHORT_BM + row;
-        const bool warp_live = x.tile * SHORT_BM + q4 * 32 < a.sq;
+        // this warp's 32 rows: (batch, head), first query row, and the
+        // column of their O in the slot (their head's 16 of the group's 64
+        // when grouped: warp q4 has head q4 of the group)
+        int xb, xh, row0, ocol = 0;
+        bool warp_live;
+        if constexpr (GRP) {
+            const GroupItem x = group_item(i, a.nblk, a.h / 4);
+            xb = x.batch;
+            xh = 4 * x.group + q4;
+            row0 = 32 * x.blk;
+            ocol = D * q4;
+            warp_live = true;
+        } else {
+            const Item x = item_of(blockIdx.x + i * gridDim.x, ntile, a.h);
+            xb = x.batch;
+            xh = x.head;
+            row0 = x.tile * SHORT_BM + q4 * 32;
+            warp_live = row0 < a.sq;
+        }
+        const int grow = row0 + static_cast<int>(lane);
         const bool ok = mbar_wait(bar(BAR_SF + sl), k & 1, g, 26);
         if (!__all_sync(0xffffffffu, ok)) return;
         tc_fence_after();
@@ -369,16 +561,16 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
         const bool row_out = warp_live && grow < a.sq;
         const float inv_l = 1.0f / l;
         const int64_t orow =
-            ((static_cast<int64_t>(x.batch) * a.sq + (row_out ? grow : 0)) * a.h + x.head) * D;
+            ((static_cast<int64_t>(xb) * a.sq + (row_out ? grow : 0)) * a.h + xh) * D;
         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + orow);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += OCH) {
             uint32_t ov[OCH];
             if (warp_live) {
                 if constexpr (OCH == 32)
-                    tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(ov));
+                    tmem_ld32(tO + ocol + c0, *reinterpret_cast<uint32_t(*)[32]>(ov));
                 else
-                    tmem_ld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
+                    tmem_ld16(tO + ocol + c0, *reinterpret_cast<uint32_t(*)[16]>(ov));
                 tmem_wait_ld();
             }
             if (c0 + OCH == D) {
@@ -404,7 +596,7 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
             }
         }
         if (row_out)
-            a.lse[(static_cast<int64_t>(x.batch) * a.h + x.head) * a.sq + grow] =
+            a.lse[(static_cast<int64_t>(xb) * a.h + xh) * a.sq + grow] =
                 (m_ref + __log2f(l)) * 0.69314718055994530942f;
     }
 }
@@ -417,7 +609,7 @@ constexpr int kShortRegsControl = 72;
 constexpr int kShortRegsSoftmax = 144;
 static_assert(4 * kShortRegsControl + 12 * kShortRegsSoftmax <= 16 * 128, "register split");
 
-template <int D, bool BF16, int NWG>
+template <int D, bool BF16, int NWG, bool GRP>
 __global__ void __launch_bounds__(128 * (NWG + 1), 1)
     fwd_short_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const ShortArgs a) {
@@ -431,9 +623,12 @@ __global__ void __launch_bounds__(128 * (NWG + 1), 1)
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const int ntile = (a.sq + SHORT_BM - 1) / SHORT_BM;
-    const int items = ntile * a.h * a.b;
-    const int n_items =
-        blockIdx.x < items ? (items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    // grouped: the CTA's (batch, group) pairs times the query blocks of each
+    const int units = GRP ? a.b * (a.h / 4) : ntile * a.h * a.b;
+    const int n_units =
+        blockIdx.x < units ? (units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int items = units;  // plain items: one per unit
+    const int n_items = GRP ? n_units * a.nblk : n_units;
 
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 4);
@@ -441,7 +636,9 @@ __global__ void __launch_bounds__(128 * (NWG + 1), 1)
         for (int i = 0; i < NUM_BARS; ++i) {
             const bool by_warps = (i >= BAR_PF && i < BAR_PF + SH_WG) ||
                                   (i >= BAR_FREE && i < BAR_FREE + SH_WG);
-            mbar_init(bar(i), by_warps ? 4u : 1u);  // one arrive per softmax warp
+            const bool by_copiers = i >= BAR_DF && i < BAR_DF + SHORT_MAX_STAGES;
+            // one arrive per softmax warp; per copying thread (diagonal tiles)
+            mbar_init(bar(i), by_warps ? 4u : (by_copiers ? 32u : 1u));
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -455,6 +652,14 @@ __global__ void __launch_bounds__(128 * (NWG + 1), 1)
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
+    if constexpr (GRP) {
+        // the zeros of every stage's block-diagonal tile (the copiers only
+        // ever write its diagonal blocks), visible to the tensor core
+        for (int st = 0; st < a.nstage; ++st)
+            for (uint32_t off = 16u * threadIdx.x; off < 128u * 128u; off += 16u * blockDim.x)
+                st_shared_zero16(tiles + st * a.stage_bytes + 32u * 128u + off);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -464,14 +669,23 @@ __global__ void __launch_bounds__(128 * (NWG + 1), 1)
     if (warp < 4) {
         if constexpr (NWG == 3) reg_dealloc<kShortRegsControl>();
         if (warp == 0) {
-            if (lane == 0 && !(a.flags & kFlagSkipLoads))
-                short_producer<D>(&tq, &tk, &tv, sbase, tiles, items, ntile, a, g);
+            if (lane == 0 && !(a.flags & kFlagSkipLoads)) {
+                if constexpr (GRP)
+                    group_producer(&tq, &tk, &tv, sbase, tiles, n_items, a.h / 4, a, g);
+                else
+                    short_producer<D>(&tq, &tk, &tv, sbase, tiles, items, ntile, a, g);
+            }
         } else if (warp == 1) {
-            if (lane == 0) short_mma<D, BF16>(sbase, tiles, tmem, n_items, a, g);
+            if (lane == 0) short_mma_s<D, BF16, GRP>(sbase, tiles, tmem, n_items, a, g);
+        } else if (warp == 3) {
+            if (lane == 0) short_mma_o<D, BF16, GRP>(sbase, tiles, tmem, n_items, a, g);
+        } else if constexpr (GRP) {
+            group_copier(sbase, tiles, n_items, a, g);
         }
     } else {
         if constexpr (NWG == 3) reg_alloc<kShortRegsSoftmax>();
-        short_softmax<D, BF16>(sbase, tmem, (warp - 4) >> 2, warp & 3, n_items, ntile, a, g);
+        short_softmax<D, BF16, GRP>(sbase, tmem, (warp - 4) >> 2, warp & 3, n_items, ntile, a,
+                                    g);
     }
 
     tc_fence_before();
@@ -480,7 +694,7 @@ __global__ void __launch_bounds__(128 * (NWG + 1), 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool BF16, int NWG>
+template <int D, bool BF16, int NWG, bool GRP>
 cudaError_t launch_short_w(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const ShortArgs &a, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -488,40 +702,72 @@ cudaError_t launch_short_w(const CUtensorMap &tq, const CUtensorMap &tk, const C
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_short_kernel<D, BF16, NWG>,
+        e = cudaFuncSetAttribute(fwd_short_kernel<D, BF16, NWG, GRP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SHORT_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    fwd_short_kernel<D, BF16, NWG>
+    fwd_short_kernel<D, BF16, NWG, GRP>
         <<<grid, 128 * (NWG + 1), SHORT_SMEM_BYTES, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool GRP>
 cudaError_t launch_short_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const ShortArgs &a, int grid, cudaStream_t stream) {
     switch (a.nslot) {
-        case 2: return launch_short_w<D, BF16, 2>(tq, tk, tv, a, grid, stream);
-        case 3: return launch_short_w<D, BF16, 3>(tq, tk, tv, a, grid, stream);
+        case 2: return launch_short_w<D, BF16, 2, GRP>(tq, tk, tv, a, grid, stream);
+        case 3: return launch_short_w<D, BF16, 3, GRP>(tq, tk, tv, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-bool short_plan(int sk, int d, ShortArgs *a) {
-    if (sk < 1 || sk > SHORT_MAX_KEYS || (d != 16 && d != 32 && d != 64)) return false;
+bool short_plan(int sq, int sk, int h, int d, bool grouped_ok, ShortArgs *a) {
+    if (sq < 1 || sk < 1 || h < 1 || sk > SHORT_MAX_KEYS || (d != 16 && d != 32 && d != 64))
+        return false;
     const int n = (sk + 31) / 32 * 32;
-    const int row_bytes = d * 2;
     const int o_off = (n / 2 + 31) / 32 * 32;
+    constexpr int avail = SHORT_SMEM_BYTES - 1024 - SH_BAR_BYTES;
+    // grouped items at head dim 16 when the heads come in fours
+    if (grouped_ok && d == 16 && h % 4 == 0) {
+        const int kv_bytes = n * 128;                       // one group K or V tile
+        const int stage_bytes = 32 * 128 + 128 * 128;       // staging block + diagonal tile
+        int w = n > o_off + 64 ? n : o_off + 64;
+        w = (w + 31) / 32 * 32;
+        int slots = 512 / w;
+        if (slots > SHORT_MAX_SLOTS) slots = SHORT_MAX_SLOTS;
+        // three kv stages when four query stages still fit, else two
+        const int nkv = 3 * 2 * kv_bytes + 4 * stage_bytes <= avail ? 3 : 2;
+        int stages = (avail - nkv * 2 * kv_bytes) / stage_bytes;
+        if (stages > SHORT_MAX_STAGES) stages = SHORT_MAX_STAGES;
+        if (stages >= 2) {
+            if (slots > stages) slots = stages;
+            a->n_keys = n;
+            a->o_off = o_off;
+            a->slot_cols = w;
+            a->nslot = slots;
+            a->kv_bytes = kv_bytes;
+            a->stage_bytes = stage_bytes;
+            a->nstage = stages;
+            a->grouped = 1;
+            a->nblk = (sq + 31) / 32;
+            a->kv_stage_bytes = 2 * kv_bytes;
+            a->nkv_stage = nkv;
+            a->q_bytes = stage_bytes;
+            return true;
+        }
+    }
+    const int row_bytes = d * 2;
     int w = n > o_off + d ? n : o_off + d;
     w = (w + 31) / 32 * 32;
     int slots = 512 / w;
     if (slots > SHORT_MAX_SLOTS) slots = SHORT_MAX_SLOTS;
     const int kv_bytes = n * row_bytes;
-    const int stage_bytes = SHORT_BM * row_bytes + 2 * kv_bytes;  // a multiple of 1024
-    int stages = (SHORT_SMEM_BYTES - 1024 - SH_BAR_BYTES) / stage_bytes;
+    const int q_bytes = SHORT_BM * row_bytes;
+    const int stage_bytes = q_bytes + 2 * kv_bytes;  // a multiple of 1024
+    int stages = avail / stage_bytes;
     if (stages > SHORT_MAX_STAGES) stages = SHORT_MAX_STAGES;
     if (stages < 1) return false;
     // the MMA issuer runs a slot's P V up to slots - 1 items behind its
@@ -534,16 +780,31 @@ bool short_plan(int sk, int d, ShortArgs *a) {
     a->kv_bytes = kv_bytes;
     a->stage_bytes = stage_bytes;
     a->nstage = stages;
+    a->grouped = 0;
+    a->nblk = 0;
+    a->kv_stage_bytes = 0;
+    a->nkv_stage = 0;
+    a->q_bytes = q_bytes;
     return true;
+}
+
+int64_t short_units(const ShortArgs &a, int64_t b, int64_t h) {
+    if (a.grouped) return b * (h / 4);
+    return b * h * ((a.sq + SHORT_BM - 1) / SHORT_BM);
 }
 
 cudaError_t launch_fwd_short(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const ShortArgs &a, int grid,
                              cudaStream_t stream) {
-#define EXATTN_SHORT_CASE(DD)                                                \
-    case DD:                                                                 \
-        return bf16 ? launch_short_t<DD, true>(tq, tk, tv, a, grid, stream)  \
-                    : launch_short_t<DD, false>(tq, tk, tv, a, grid, stream);
+#define EXATTN_SHORT_CASE(DD)                                                       \
+    case DD:                                                                        \
+        return bf16 ? launch_short_t<DD, true, false>(tq, tk, tv, a, grid, stream)  \
+                    : launch_short_t<DD, false, false>(tq, tk, tv, a, grid, stream);
+    if (a.grouped) {
+        if (d != 16) return cudaErrorInvalidValue;
+        return bf16 ? launch_short_t<16, true, true>(tq, tk, tv, a, grid, stream)
+                    : launch_short_t<16, false, true>(tq, tk, tv, a, grid, stream);
+    }
     switch (d) {
         EXATTN_SHORT_CASE(16)
         EXATTN_SHORT_CASE(32)

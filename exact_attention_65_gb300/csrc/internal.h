@@ -84,11 +84,22 @@ struct ShortArgs {
     // O accumulator's column in a slot, slot width, slots in use, bytes of
     // one K or V tile (N rows), bytes of one stage (Q + K + V), stages
     int n_keys, o_off, slot_cols, nslot, kv_bytes, stage_bytes, nstage;
+    // Grouped items (head dim 16, h a multiple of 4; fwd_short.cu): a work
+    // item is one 32-row query block of a group of four consecutive heads;
+    // the group's K and V tiles (kv_bytes each, 128-byte rows) sit in a ring
+    // of nkv_stage stages of kv_stage_bytes after the item stages. nblk:
+    // query blocks per head. q_bytes: the query part of an item stage.
+    int grouped, nblk, kv_stage_bytes, nkv_stage, q_bytes;
 };
 
-// Fills the plan fields of `a` for sk keys and head dim d; false if the
-// short forward does not take this shape.
-bool short_plan(int sk, int d, ShortArgs *a);
+// Fills the plan fields of `a` for sq query rows, sk keys, h heads and
+// head dim d (grouped items only if grouped_ok); false if the short
+// forward does not take this shape.
+bool short_plan(int sq, int sk, int h, int d, bool grouped_ok, ShortArgs *a);
+
+// What the persistent grid deals out over b batches and h heads: plain
+// items, or (batch, group of four heads) pairs when grouped.
+int64_t short_units(const ShortArgs &a, int64_t b, int64_t h);
 
 cudaError_t launch_fwd_short(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const ShortArgs &a, int grid,

@@ -6,7 +6,8 @@ kernel, which must agree with the oracle too.
 
 Shapes: key counts on both sides of every 32-column chunk edge and of the
 slot widths (1, 5, 31, 32, 33, 100, 128, 150, 160, 161, 192, 224, 255, 256),
-query counts from one row to several ragged 128-row tiles, every head dim,
+query counts from one row to several ragged 128-row tiles, grouped items
+(head dim 16, heads in fours: 32-row query blocks of four heads), every head dim,
 both dtypes, zero and negative scale, and far more tiles than SMs so that
 every TMEM slot and shared-memory stage is reused many times. Tolerance as
 everywhere: max |O - O_ref| <= 2e-2, max |LSE - LSE_ref| <= 1e-3.
@@ -55,6 +56,41 @@ def test_query_counts_and_dtypes(gpu, oracle_mod, sq, dtype):
     o_ref, lse_ref = oracle_mod.attention(q, k, v, scale)
     o, lse = _run(gpu, q, k, v, scale)
     compare(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("b,sq,h", [(48, 20, 4), (24, 1, 8), (48, 33, 4), (16, 64, 12), (48, 97, 4),
+                                    (24, 150, 8), (48, 200, 4), (24, 256, 8), (32, 150, 6)])
+@pytest.mark.parametrize("sk", [37, 150, 256])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_grouped_heads(gpu, oracle_mod, b, sq, h, sk, dtype):
+    """Head dim 16 with the heads in groups of four and more one-head tiles
+    than SMs: items of one 32-row query block of four heads, the group's K
+    and V loaded once for all of its blocks (one, two, several and ragged
+    blocks per head, one key chunk to the most keys, several groups and
+    batches); h = 6 takes the one-head-per-item path."""
+    q, k, v = workloads.make_qkv(b, sq, sk, h, 16, dtype, seed=300 + sq + sk + h)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, 0.25)
+    o, lse = _run(gpu, q, k, v, 0.25)
+    compare(o, lse, o_ref, lse_ref)
+
+
+def test_grouped_heads_stay_apart(gpu, oracle_mod):
+    """The four heads of a group share one 128-row tile but meet only their
+    own keys and values: heads with scores and values of very different
+    sizes side by side each match the oracle."""
+    b, sq, sk, h, d = 48, 20, 90, 4, 16
+    q, k, v = workloads.make_qkv(b, sq, sk, h, d, torch.float16, seed=77)
+    k = k.float()
+    v = v.float()
+    k[:, :, 0] *= 8.0
+    v[:, :, 1] *= 50.0
+    k[:, :, 2] *= 0.05
+    k, v = k.to(torch.float16), v.to(torch.float16)
+    o_ref, lse_ref = oracle_mod.attention(q, k, v, 0.25)
+    o, lse = _run(gpu, q, k, v, 0.25)
+    # head 1's values are 50 times larger: its O tolerance scales with them
+    compare(o[:, :, [0, 2, 3]], lse, o_ref[:, :, [0, 2, 3]], lse_ref)
+    compare(o[:, :, 1:2] / 50.0, lse[:, 1:2], o_ref[:, :, 1:2] / 50.0, lse_ref[:, 1:2])
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.4, 1.3])
@@ -119,11 +155,14 @@ def test_output_only_16_byte_aligned(gpu, oracle_mod):
     compare(out, lse, o_ref, lse_ref)
 
 
-def test_timeout_and_recovery(gpu):
+@pytest.mark.parametrize("h", [2, 4])
+def test_timeout_and_recovery(gpu, h):
     """ATTN_DEBUG_SKIP_LOADS: the producer issues nothing, the first wait on
     a full stage runs out after its bound, the kernel returns, the status
-    reports it, and the next call works."""
-    q, k, v = (t.cuda() for t in workloads.make_qkv(1, 64, 100, 2, 16, torch.float16, seed=3))
+    reports it, and the next call works (h = 4: grouped items, whose copier
+    warps wait on the same stages)."""
+    b = 1 if h == 2 else 48  # h = 4, b = 48: 192 one-head tiles, so grouped items
+    q, k, v = (t.cuda() for t in workloads.make_qkv(b, 64, 100, h, 16, torch.float16, seed=3))
     assert gpu.attn_get_device_status() == gpu.ATTN_OK
     gpu.attn_debug_set_flags(gpu.ATTN_DEBUG_SKIP_LOADS)
     try:

@@ -55,6 +55,10 @@ typedef enum {
  * softmax, times V; the call flash_attn_func(q, k, v) of item 5), computed
  * tile by tile with the online softmax of section 3.3. Non-causal, no
  * dropout. dtype selects fp16 or bf16 for q, k, v and o.
+ * Inputs are taken to be finite: at d = 16 with h a multiple of 4, heads
+ * are computed four at a time in one tile, and a key holding an infinity
+ * or a NaN also turns the rows of the other three heads of its group to
+ * NaN.
  * Returns ATTN_OK once the kernel is enqueued on `stream`.
  */
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

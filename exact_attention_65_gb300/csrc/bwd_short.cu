@@ -26,10 +26,13 @@
 // Persistent CTAs (one per SM) take items round-robin:
 //   warp 0        TMA producer: Q, dO, K, V of an item into a stage (two
 //                 stages at d = 16, one at d = 32).
-//   warp 1        TMEM owner and MMA issuer (one thread).
+//   warp 1        TMEM owner; issues S, dP and dQ MMAs (one thread).
 //   warp 2        stages each item's LSE and D rows in shared memory ahead
 //                 of its use (the elementwise warps would otherwise start
 //                 each item with a global load of them).
+//   warp 3        issues the dV and dK MMAs (one thread), so that a tile's
+//                 dQ and the next tile's S and dP go out beside them rather
+//                 than after them.
 //   warps 4-11    elementwise: group g (warps 4 + 4g .. 7 + 4g) holds all
 //                 128 lanes and takes the 16-key chunks c with c % 2 == g;
 //                 group g also writes dK and dV of key M tile g.
@@ -68,7 +71,7 @@ struct SbGeom {
     static constexpr int OFF_LD = OFF_DS + SB_PDS_BYTES;
     static constexpr int OFF_BAR = OFF_LD + STAGES * 2 * SBWD_MAX_Q * 4;
     static constexpr int BAR_INF = 0;              // [2] an item's inputs landed
-    static constexpr int BAR_INE = BAR_INF + 2;    // [2] its last MMA has read them
+    static constexpr int BAR_INE = BAR_INF + 2;    // [2] its last MMAs (both issuers) read them
     static constexpr int BAR_SF = BAR_INE + 2;     // a tile's S and dP in TMEM
     static constexpr int BAR_PF = BAR_SF + 1;      // its P and dS written (8 warps)
     static constexpr int BAR_PFREE = BAR_PF + 1;   // its dV / dK MMAs have read them
@@ -77,8 +80,8 @@ struct SbGeom {
     static constexpr int BAR_KVF = BAR_QE + 1;     // the item's dK and dV in TMEM
     static constexpr int BAR_KVE = BAR_KVF + 1;    // read out (8 warps)
     static constexpr int BAR_LDF = BAR_KVE + 1;    // [2] an item's LSE and D staged (warp 2)
-    static constexpr int BAR_DONE = BAR_LDF + 2;
-    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int BAR_DONE = BAR_LDF + 2;   // [2] each issuer's MMAs complete
+    static constexpr int NUM_BARS = BAR_DONE + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(OFF_P % 1024 == 0, "P and dS panels on swizzle-atom boundaries");
@@ -227,20 +230,34 @@ __device__ __forceinline__ void sb_issue_kv_n(int steps, uint32_t t_dv, uint32_t
     }
 }
 
+// Waits until every MMA this thread issued has completed (TMEM is released
+// after both issuers have done so).
+__device__ __forceinline__ void sb_drain(uint32_t done_bar, const WaitGuard &g, uint32_t site) {
+    mma_commit(done_bar);
+    WaitGuard drain = g;
+    uint32_t no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(done_bar, 0, drain, site);
+}
+
+// The MMAs are issued by two threads. Warp 1: per tile S and dP, then (once
+// P and dS are made) dQ, then the next tile's S and dP; warp 3: per tile the
+// dV and dK MMAs, which read P and dS from the shared-memory panels and
+// release them (p_free). One thread issuing all of them sent a tile's 10 dQ
+// and 32 dV / dK MMAs (N = 16) one after the other, and the next tile's S and
+// dP only after those. Nothing orders the two streams but the barriers: the
+// panels are rewritten only after p_free, S and dP only after this thread's
+// own dQ has read dS out of S's columns, and the accumulators are disjoint.
 template <int D, bool BF16>
-__device__ __forceinline__ void sb_mma(uint32_t sbase, uint32_t tmem, int n_items,
-                                       const SbPlan &p, int sq, const WaitGuard &g) {
+__device__ __forceinline__ void sb_mma_sq(uint32_t sbase, uint32_t tmem, int n_items,
+                                          const SbPlan &p, const WaitGuard &g) {
     using G = SbGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     const uint32_t idesc_s = mma_idesc_f16(SB_QT, p.n, BF16, false, false);
     constexpr uint32_t idesc_q = mma_idesc_f16(SB_QT, D, BF16, false, true);  // A TMEM, B MN-major
-    constexpr uint32_t idesc_kv = mma_idesc_f16(SB_QT, D, BF16, true, true);  // A, B MN-major
-    // stage 0's K-major and MN-major views; P and dS panels (MN-major A:
-    // the leading offset steps 64 keys, the stride offset 8 query rows)
+    // stage 0's K-major and MN-major views
     const uint64_t kmaj = smem_desc(sbase, 16, G::SBO, G::LAYOUT);
     const uint64_t mnmaj = smem_desc(sbase, G::TQ_BYTES, G::SBO, G::LAYOUT);
-    const uint64_t pdesc = smem_desc(sbase + G::OFF_P, SB_PANEL_BYTES, 1024, kLayoutSw128);
-    const uint64_t dsdesc = smem_desc(sbase + G::OFF_DS, SB_PANEL_BYTES, 1024, kLayoutSw128);
     const uint32_t t_s = tmem, t_dp = tmem + p.c_dp, t_dq = tmem + p.c_dq;
     int n_tile = 0;
     for (int i = 0; i < n_items; ++i) {
@@ -275,6 +292,36 @@ __device__ __forceinline__ void sb_mma(uint32_t sbase, uint32_t tmem, int n_item
             tc_fence_after();
             sb_issue_dq_n<D>(p.n / 16, t_dq, t_s, mnmaj + so + o_k, idesc_q);
             mma_commit(bar(G::BAR_QF));
+        }
+        if (!ok) break;
+        mma_commit(bar(G::BAR_INE + st));
+    }
+    sb_drain(bar(G::BAR_DONE), g, 46);
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void sb_mma_kv(uint32_t sbase, uint32_t tmem, int n_items,
+                                          const SbPlan &p, int sq, const WaitGuard &g) {
+    using G = SbGeom<D>;
+    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
+    constexpr uint32_t idesc_kv = mma_idesc_f16(SB_QT, D, BF16, true, true);  // A, B MN-major
+    // stage 0's MN-major view; P and dS panels (MN-major A: the leading
+    // offset steps 64 keys, the stride offset 8 query rows)
+    const uint64_t mnmaj = smem_desc(sbase, G::TQ_BYTES, G::SBO, G::LAYOUT);
+    const uint64_t pdesc = smem_desc(sbase + G::OFF_P, SB_PANEL_BYTES, 1024, kLayoutSw128);
+    const uint64_t dsdesc = smem_desc(sbase + G::OFF_DS, SB_PANEL_BYTES, 1024, kLayoutSw128);
+    int n_tile = 0;
+    for (int i = 0; i < n_items; ++i) {
+        const int st = i % G::STAGES;
+        const uint32_t so = (st * G::STAGE_BYTES) >> 4;
+        const uint32_t o_do = G::TQ_BYTES >> 4;
+        bool ok = true;
+        for (int qt = 0; qt < p.nqt; ++qt, ++n_tile) {
+            const uint32_t oq = (qt * SB_QT * G::RB) >> 4;
+            if (!mbar_wait(bar(G::BAR_PF), n_tile & 1, g, 54)) {
+                ok = false;
+                break;
+            }
             // dV += P^T dO_t, dK += dS^T Q_t per 128-key M tile, 16 query rows
             // per MMA; the item's first tile overwrites what the previous
             // item's epilogue has read out
@@ -297,12 +344,7 @@ __device__ __forceinline__ void sb_mma(uint32_t sbase, uint32_t tmem, int n_item
         mma_commit(bar(G::BAR_INE + st));
         mma_commit(bar(G::BAR_KVF));
     }
-    // no MMA may still be running when TMEM is released
-    mma_commit(bar(G::BAR_DONE));
-    WaitGuard drain = g;
-    uint32_t no_abort = 0;
-    drain.abort = &no_abort;
-    mbar_wait(bar(G::BAR_DONE), 0, drain, 46);
+    sb_drain(bar(G::BAR_DONE + 1), g, 53);
 }
 
 // Stores COLS fp32 TMEM columns of this thread's lane, times mul, as 16-bit.
@@ -484,8 +526,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i) {
             const bool by_warps = i == G::BAR_PF || i == G::BAR_QE || i == G::BAR_KVE;
+            const bool by_issuers = i == G::BAR_INE || i == G::BAR_INE + 1;  // both commit
             // BAR_LDF: one arrive by warp 2's lane 0
-            mbar_init(bar(i), by_warps ? static_cast<uint32_t>(SB_EW_WARPS) : 1u);
+            mbar_init(bar(i), by_warps ? static_cast<uint32_t>(SB_EW_WARPS) : (by_issuers ? 2u : 1u));
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -510,7 +553,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         if (lane == 0 && !(a.flags & kFlagSkipLoads))
             sb_producer<D>(&tq, &tk, &tv, &tdo, sbase, items, p, a, g);
     } else if (warp == 1) {
-        if (lane == 0) sb_mma<D, BF16>(sbase, tmem, n_items, p, a.sq, g);
+        if (lane == 0) sb_mma_sq<D, BF16>(sbase, tmem, n_items, p, g);
+    } else if (warp == 3) {
+        if (lane == 0) sb_mma_kv<D, BF16>(sbase, tmem, n_items, p, a.sq, g);
     } else if (warp == 2) {
         sb_stage_ld<D>(smem, sbase, items, a, g);
     } else if (warp >= 4) {

@@ -24,15 +24,16 @@
 //   second pass.
 //
 // Persistent CTAs (one per SM) take items round-robin:
-//   warp 0        TMA producer: Q, dO, K, V of an item into a stage (two
-//                 stages at d = 16, one at d = 32).
-//   warp 1        TMEM owner; issues S, dP and dQ MMAs (one thread).
-//   warp 2        stages each item's LSE and D rows in shared memory ahead
-//                 of its use (the elementwise warps would otherwise start
+//   warp 0        TMA producer (lane 0): Q, dO, K, V of an item into a stage
+//                 (two stages at d = 16, one at d = 32); then the whole warp
+//                 stages the item's LSE and D rows in shared memory ahead of
+//                 their use (the elementwise warps would otherwise start
 //                 each item with a global load of them).
-//   warp 3        issues the dV and dK MMAs (one thread), so that a tile's
-//                 dQ and the next tile's S and dP go out beside them rather
-//                 than after them.
+//   warp 1        TMEM owner; issues S, dP and dQ MMAs (one thread).
+//   warp 2        issues the dK MMAs (one thread).
+//   warp 3        issues the dV MMAs (one thread): a tile's dQ, dK and dV
+//                 and the next tile's S and dP go out side by side rather
+//                 than one after another.
 //   warps 4-11    elementwise: group g (warps 4 + 4g .. 7 + 4g) holds all
 //                 128 lanes and takes the 16-key chunks c with c % 2 == g;
 //                 group g also writes dK and dV of key M tile g.
@@ -71,17 +72,17 @@ struct SbGeom {
     static constexpr int OFF_LD = OFF_DS + SB_PDS_BYTES;
     static constexpr int OFF_BAR = OFF_LD + STAGES * 2 * SBWD_MAX_Q * 4;
     static constexpr int BAR_INF = 0;              // [2] an item's inputs landed
-    static constexpr int BAR_INE = BAR_INF + 2;    // [2] its last MMAs (both issuers) read them
+    static constexpr int BAR_INE = BAR_INF + 2;    // [2] its last MMAs (all 3 issuers) read them
     static constexpr int BAR_SF = BAR_INE + 2;     // a tile's S and dP in TMEM
     static constexpr int BAR_PF = BAR_SF + 1;      // its P and dS written (8 warps)
-    static constexpr int BAR_PFREE = BAR_PF + 1;   // its dV / dK MMAs have read them
+    static constexpr int BAR_PFREE = BAR_PF + 1;   // its dV and dK MMAs have read them (2)
     static constexpr int BAR_QF = BAR_PFREE + 1;   // its dQ in TMEM
     static constexpr int BAR_QE = BAR_QF + 1;      // dQ read out (8 warps)
-    static constexpr int BAR_KVF = BAR_QE + 1;     // the item's dK and dV in TMEM
+    static constexpr int BAR_KVF = BAR_QE + 1;     // the item's dK and dV in TMEM (2)
     static constexpr int BAR_KVE = BAR_KVF + 1;    // read out (8 warps)
-    static constexpr int BAR_LDF = BAR_KVE + 1;    // [2] an item's LSE and D staged (warp 2)
-    static constexpr int BAR_DONE = BAR_LDF + 2;   // [2] each issuer's MMAs complete
-    static constexpr int NUM_BARS = BAR_DONE + 2;
+    static constexpr int BAR_LDF = BAR_KVE + 1;    // [2] an item's LSE and D staged (warp 0)
+    static constexpr int BAR_DONE = BAR_LDF + 2;   // [3] each issuer's MMAs complete
+    static constexpr int NUM_BARS = BAR_DONE + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(OFF_P % 1024 == 0, "P and dS panels on swizzle-atom boundaries");
@@ -116,51 +117,39 @@ __device__ __forceinline__ uint32_t sb_pack(float lo, float hi) {
         return cvt_pack_f16(lo, hi);
 }
 
+// Warp 0. Lane 0 waits for an item's stage and loads its Q, dO, K and V;
+// then the warp writes LSE * log2(e) and D of every query row of the item
+// into the stage (rows past sq get LSE = +inf, hence P = 0, and D = 0).
 template <int D>
 __device__ __forceinline__ void sb_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                             const CUtensorMap *tv, const CUtensorMap *tdo,
-                                            uint32_t sbase, int items, const SbPlan &p,
-                                            const BwdArgs &a, const WaitGuard &g) {
-    using G = SbGeom<D>;
-    auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
-    const uint32_t bytes = 2u * (p.nqt * SB_QT) * G::RB + 2u * p.n * G::RB;
-    int n = 0;
-    for (int it = blockIdx.x; it < items; it += gridDim.x, ++n) {
-        const int head = it % a.h, batch = it / a.h;
-        const int st = n % G::STAGES;
-        if (!mbar_wait(bar(G::BAR_INE + st), ((n / G::STAGES) & 1) ^ 1, g, 40)) break;
-        mbar_arrive_expect_tx(bar(G::BAR_INF + st), bytes);
-        const uint32_t dst = sbase + st * G::STAGE_BYTES;
-        tma_load_4d(dst, tq, bar(G::BAR_INF + st), 0, head, 0, batch);
-        tma_load_4d(dst + G::TQ_BYTES, tdo, bar(G::BAR_INF + st), 0, head, 0, batch);
-        tma_load_4d(dst + 2 * G::TQ_BYTES, tk, bar(G::BAR_INF + st), 0, head, 0, batch);
-        tma_load_4d(dst + 2 * G::TQ_BYTES + G::TK_BYTES, tv, bar(G::BAR_INF + st), 0, head, 0,
-                    batch);
-    }
-    // never leave the CTA with a copy still landing in shared memory
-    WaitGuard drain = g;
-    uint32_t no_abort = 0;
-    drain.abort = &no_abort;
-    for (int m = (n > G::STAGES ? n - G::STAGES : 0); m < n; ++m)
-        mbar_wait(bar(G::BAR_INF + m % G::STAGES), (m / G::STAGES) & 1, drain, 41);
-}
-
-// Warp 2: LSE * log2(e) and D of every query row of the CTA's items into the
-// item's stage, as soon as the stage's previous item is done with it (rows
-// past sq get LSE = +inf, hence P = 0, and D = 0).
-template <int D>
-__device__ __forceinline__ void sb_stage_ld(uint8_t *smem, uint32_t sbase, int items,
-                                            const BwdArgs &a, const WaitGuard &g) {
+                                            uint8_t *smem, uint32_t sbase, int items,
+                                            const SbPlan &p, const BwdArgs &a,
+                                            const WaitGuard &g) {
     using G = SbGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     constexpr float kLog2e = 1.4426950408889634f;
     const uint32_t lane = threadIdx.x & 31;
-    const int rows = (a.sq + SB_QT - 1) / SB_QT * SB_QT;
+    const uint32_t bytes = 2u * (p.nqt * SB_QT) * G::RB + 2u * p.n * G::RB;
+    const int rows = p.nqt * SB_QT;
     int n = 0;
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+        const int head = it % a.h, batch = it / a.h;
         const int st = n % G::STAGES;
-        const bool ok = mbar_wait(bar(G::BAR_INE + st), ((n / G::STAGES) & 1) ^ 1, g, 51);
-        if (!__all_sync(0xffffffffu, ok)) return;
+        bool ok = true;
+        if (lane == 0) {
+            ok = mbar_wait(bar(G::BAR_INE + st), ((n / G::STAGES) & 1) ^ 1, g, 40);
+            if (ok) {
+                mbar_arrive_expect_tx(bar(G::BAR_INF + st), bytes);
+                const uint32_t dst = sbase + st * G::STAGE_BYTES;
+                tma_load_4d(dst, tq, bar(G::BAR_INF + st), 0, head, 0, batch);
+                tma_load_4d(dst + G::TQ_BYTES, tdo, bar(G::BAR_INF + st), 0, head, 0, batch);
+                tma_load_4d(dst + 2 * G::TQ_BYTES, tk, bar(G::BAR_INF + st), 0, head, 0, batch);
+                tma_load_4d(dst + 2 * G::TQ_BYTES + G::TK_BYTES, tv, bar(G::BAR_INF + st), 0,
+                            head, 0, batch);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const int64_t base = static_cast<int64_t>(it) * a.sq;  // (batch, head) = it
         float *ld = reinterpret_cast<float *>(smem + G::OFF_LD) + st * 2 * SBWD_MAX_Q;
         for (int r = lane; r < rows; r += 32) {
@@ -170,6 +159,14 @@ __device__ __forceinline__ void sb_stage_ld(uint8_t *smem, uint32_t sbase, int i
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(G::BAR_LDF + st));
+    }
+    // never leave the CTA with a copy still landing in shared memory
+    if (lane == 0) {
+        WaitGuard drain = g;
+        uint32_t no_abort = 0;
+        drain.abort = &no_abort;
+        for (int m = (n > G::STAGES ? n - G::STAGES : 0); m < n; ++m)
+            mbar_wait(bar(G::BAR_INF + m % G::STAGES), (m / G::STAGES) & 1, drain, 41);
     }
 }
 
@@ -197,36 +194,31 @@ __device__ __forceinline__ void sb_issue_dq_n(int steps, uint32_t t_dq, uint32_t
     }
 }
 
-// dV += P^T dO_t and dK += dS^T Q_t for key M tile mt over the tile's
+// dV += P^T dO_t (or dK += dS^T Q_t) for key M tile mt over the tile's
 // first 16 STEPS query rows (rows past sq hold P = dS = 0 and are skipped),
-// one straight-line run; acc0 = 0 overwrites (the item's first tile).
+// one straight-line run; acc0 = 0 overwrites (the item's first tile). a is
+// the P (or dS) panel pair of the M tile, b dO_t (or Q_t).
 template <int D, int STEPS>
-__device__ __forceinline__ void sb_issue_kv(uint32_t t_dv, uint32_t t_dk, uint64_t pa, uint64_t dsa,
-                                            uint64_t dob, uint64_t qb, uint32_t idesc,
+__device__ __forceinline__ void sb_issue_kv(uint32_t t_acc, uint64_t a, uint64_t b, uint32_t idesc,
                                             uint32_t acc0) {
 #pragma unroll
     for (int kk = 0; kk < STEPS; ++kk)
-        mma_ss(t_dv, pa + ((kk * 2048) >> 4), dob + ((kk * 16 * SbGeom<D>::RB) >> 4), idesc,
-               (acc0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-    for (int kk = 0; kk < STEPS; ++kk)
-        mma_ss(t_dk, dsa + ((kk * 2048) >> 4), qb + ((kk * 16 * SbGeom<D>::RB) >> 4), idesc,
+        mma_ss(t_acc, a + ((kk * 2048) >> 4), b + ((kk * 16 * SbGeom<D>::RB) >> 4), idesc,
                (acc0 || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
-__device__ __forceinline__ void sb_issue_kv_n(int steps, uint32_t t_dv, uint32_t t_dk,
-                                              uint64_t pa, uint64_t dsa, uint64_t dob,
-                                              uint64_t qb, uint32_t idesc, uint32_t acc0) {
+__device__ __forceinline__ void sb_issue_kv_n(int steps, uint32_t t_acc, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t acc0) {
     switch (steps) {
-        case 1: sb_issue_kv<D, 1>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 2: sb_issue_kv<D, 2>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 3: sb_issue_kv<D, 3>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 4: sb_issue_kv<D, 4>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 5: sb_issue_kv<D, 5>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 6: sb_issue_kv<D, 6>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        case 7: sb_issue_kv<D, 7>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
-        default: sb_issue_kv<D, 8>(t_dv, t_dk, pa, dsa, dob, qb, idesc, acc0); break;
+        case 1: sb_issue_kv<D, 1>(t_acc, a, b, idesc, acc0); break;
+        case 2: sb_issue_kv<D, 2>(t_acc, a, b, idesc, acc0); break;
+        case 3: sb_issue_kv<D, 3>(t_acc, a, b, idesc, acc0); break;
+        case 4: sb_issue_kv<D, 4>(t_acc, a, b, idesc, acc0); break;
+        case 5: sb_issue_kv<D, 5>(t_acc, a, b, idesc, acc0); break;
+        case 6: sb_issue_kv<D, 6>(t_acc, a, b, idesc, acc0); break;
+        case 7: sb_issue_kv<D, 7>(t_acc, a, b, idesc, acc0); break;
+        default: sb_issue_kv<D, 8>(t_acc, a, b, idesc, acc0); break;
     }
 }
 
@@ -240,14 +232,15 @@ __device__ __forceinline__ void sb_drain(uint32_t done_bar, const WaitGuard &g, 
     mbar_wait(done_bar, 0, drain, site);
 }
 
-// The MMAs are issued by two threads. Warp 1: per tile S and dP, then (once
-// P and dS are made) dQ, then the next tile's S and dP; warp 3: per tile the
-// dV and dK MMAs, which read P and dS from the shared-memory panels and
-// release them (p_free). One thread issuing all of them sent a tile's 10 dQ
-// and 32 dV / dK MMAs (N = 16) one after the other, and the next tile's S and
-// dP only after those. Nothing orders the two streams but the barriers: the
-// panels are rewritten only after p_free, S and dP only after this thread's
-// own dQ has read dS out of S's columns, and the accumulators are disjoint.
+// The MMAs are issued by three threads. Warp 1: per tile S and dP, then
+// (once P and dS are made) dQ, then the next tile's S and dP; warp 3 the dV
+// MMAs and warp 2 the dK MMAs of each tile, which read P and dS from the
+// shared-memory panels and release them (p_free, once both have). One thread
+// issuing all of them sent a tile's 10 dQ and 32 dV / dK MMAs (N = 16) one
+// after the other, and the next tile's S and dP only after those. Nothing
+// orders the streams but the barriers: the panels are rewritten only after
+// p_free, S and dP only after warp 1's own dQ has read dS out of S's
+// columns, and the accumulators are disjoint.
 template <int D, bool BF16>
 __device__ __forceinline__ void sb_mma_sq(uint32_t sbase, uint32_t tmem, int n_items,
                                           const SbPlan &p, const WaitGuard &g) {
@@ -299,32 +292,33 @@ __device__ __forceinline__ void sb_mma_sq(uint32_t sbase, uint32_t tmem, int n_i
     sb_drain(bar(G::BAR_DONE), g, 46);
 }
 
-template <int D, bool BF16>
+// DK = false: dV += P^T dO_t; DK = true: dK += dS^T Q_t.
+template <int D, bool BF16, bool DK>
 __device__ __forceinline__ void sb_mma_kv(uint32_t sbase, uint32_t tmem, int n_items,
                                           const SbPlan &p, int sq, const WaitGuard &g) {
     using G = SbGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
     constexpr uint32_t idesc_kv = mma_idesc_f16(SB_QT, D, BF16, true, true);  // A, B MN-major
-    // stage 0's MN-major view; P and dS panels (MN-major A: the leading
+    // stage 0's MN-major view; the P or dS panels (MN-major A: the leading
     // offset steps 64 keys, the stride offset 8 query rows)
     const uint64_t mnmaj = smem_desc(sbase, G::TQ_BYTES, G::SBO, G::LAYOUT);
-    const uint64_t pdesc = smem_desc(sbase + G::OFF_P, SB_PANEL_BYTES, 1024, kLayoutSw128);
-    const uint64_t dsdesc = smem_desc(sbase + G::OFF_DS, SB_PANEL_BYTES, 1024, kLayoutSw128);
+    const uint64_t adesc =
+        smem_desc(sbase + (DK ? G::OFF_DS : G::OFF_P), SB_PANEL_BYTES, 1024, kLayoutSw128);
+    const uint32_t t_acc = tmem + (DK ? p.c_dk : p.c_dv);
     int n_tile = 0;
     for (int i = 0; i < n_items; ++i) {
         const int st = i % G::STAGES;
-        const uint32_t so = (st * G::STAGE_BYTES) >> 4;
-        const uint32_t o_do = G::TQ_BYTES >> 4;
+        // B: Q_t for dK, dO_t for dV
+        const uint32_t ob = (st * G::STAGE_BYTES + (DK ? 0 : G::TQ_BYTES)) >> 4;
         bool ok = true;
         for (int qt = 0; qt < p.nqt; ++qt, ++n_tile) {
             const uint32_t oq = (qt * SB_QT * G::RB) >> 4;
-            if (!mbar_wait(bar(G::BAR_PF), n_tile & 1, g, 54)) {
+            if (!mbar_wait(bar(G::BAR_PF), n_tile & 1, g, DK ? 55 : 54)) {
                 ok = false;
                 break;
             }
-            // dV += P^T dO_t, dK += dS^T Q_t per 128-key M tile, 16 query rows
-            // per MMA; the item's first tile overwrites what the previous
-            // item's epilogue has read out
+            // per 128-key M tile, 16 query rows per MMA; the item's first
+            // tile overwrites what the previous item's epilogue has read out
             if (qt == 0 && i > 0 && !mbar_wait(bar(G::BAR_KVE), (i - 1) & 1, g, 45)) {
                 ok = false;
                 break;
@@ -332,19 +326,17 @@ __device__ __forceinline__ void sb_mma_kv(uint32_t sbase, uint32_t tmem, int n_i
             tc_fence_after();
             const int rows = min(SB_QT, sq - qt * SB_QT);  // the tile's query rows
             const int ksteps = (rows + 15) / 16;
-            for (int mt = 0; mt < p.nmk; ++mt) {
-                const uint32_t om = (2 * mt * SB_PANEL_BYTES) >> 4;
-                sb_issue_kv_n<D>(ksteps, tmem + p.c_dv + mt * SB_COL_W, tmem + p.c_dk + mt * SB_COL_W,
-                                 pdesc + om, dsdesc + om, mnmaj + so + o_do + oq, mnmaj + so + oq,
-                                 idesc_kv, qt > 0 ? 1u : 0u);
-            }
+            for (int mt = 0; mt < p.nmk; ++mt)
+                sb_issue_kv_n<D>(ksteps, t_acc + mt * SB_COL_W,
+                                 adesc + ((2 * mt * SB_PANEL_BYTES) >> 4), mnmaj + ob + oq, idesc_kv,
+                                 qt > 0 ? 1u : 0u);
             mma_commit(bar(G::BAR_PFREE));
         }
         if (!ok) break;
         mma_commit(bar(G::BAR_INE + st));
         mma_commit(bar(G::BAR_KVF));
     }
-    sb_drain(bar(G::BAR_DONE + 1), g, 53);
+    sb_drain(bar(G::BAR_DONE + (DK ? 2 : 1)), g, DK ? 56 : 53);
 }
 
 // Stores COLS fp32 TMEM columns of this thread's lane, times mul, as 16-bit.
@@ -526,9 +518,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < G::NUM_BARS; ++i) {
             const bool by_warps = i == G::BAR_PF || i == G::BAR_QE || i == G::BAR_KVE;
-            const bool by_issuers = i == G::BAR_INE || i == G::BAR_INE + 1;  // both commit
-            // BAR_LDF: one arrive by warp 2's lane 0
-            mbar_init(bar(i), by_warps ? static_cast<uint32_t>(SB_EW_WARPS) : (by_issuers ? 2u : 1u));
+            // commits of all three issuers (the stages), of the dV and dK
+            // issuers (the panels, the item's dK and dV); BAR_LDF: one
+            // arrive by warp 0's lane 0
+            const uint32_t n_arrive = by_warps ? static_cast<uint32_t>(SB_EW_WARPS)
+                                      : (i == G::BAR_INE || i == G::BAR_INE + 1) ? 3u
+                                      : (i == G::BAR_PFREE || i == G::BAR_KVF)   ? 2u
+                                                                                 : 1u;
+            mbar_init(bar(i), n_arrive);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -550,14 +547,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     const WaitGuard g{abort_flag, a.status, kKernBwd};
 
     if (warp == 0) {
-        if (lane == 0 && !(a.flags & kFlagSkipLoads))
-            sb_producer<D>(&tq, &tk, &tv, &tdo, sbase, items, p, a, g);
+        if (!(a.flags & kFlagSkipLoads))
+            sb_producer<D>(&tq, &tk, &tv, &tdo, smem, sbase, items, p, a, g);
     } else if (warp == 1) {
         if (lane == 0) sb_mma_sq<D, BF16>(sbase, tmem, n_items, p, g);
-    } else if (warp == 3) {
-        if (lane == 0) sb_mma_kv<D, BF16>(sbase, tmem, n_items, p, a.sq, g);
     } else if (warp == 2) {
-        sb_stage_ld<D>(smem, sbase, items, a, g);
+        if (lane == 0) sb_mma_kv<D, BF16, true>(sbase, tmem, n_items, p, a.sq, g);
+    } else if (warp == 3) {
+        if (lane == 0) sb_mma_kv<D, BF16, false>(sbase, tmem, n_items, p, a.sq, g);
     } else if (warp >= 4) {
         sb_elementwise<D, BF16>(smem, sbase, tmem, warp & 3, (warp - 4) >> 2, n_items, p, a, g);
     }

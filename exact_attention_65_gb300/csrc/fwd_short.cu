@@ -11,11 +11,13 @@
 // which is section 3.3's online softmax with a single block.
 //
 // A work item is one 128-row query tile of one (batch, head) against all of
-// its keys. Persistent CTAs (one per SM) deal their items to two or three
-// TMEM slots, so several items are in flight per SM and the latency chain of each
+// its keys (or, grouped, one 32-row query block of four heads: below).
+// Persistent CTAs (one per SM) deal their items to two or three TMEM slots,
+// so several items are in flight per SM and the latency chain of each
 // (loads, QK^T, softmax, PV, store) overlaps the others':
 //   warp 0        TMA producer: Q tile, K and V of the item into a ring of
-//                 shared-memory stages (packed items: idle).
+//                 shared-memory stages (grouped: the query block of the
+//                 item, and the group's K and V once per group).
 //   warp 1        TMEM owner; issues every QK^T MMA (one thread): S = Q K^T
 //                 into the item's slot.
 //   warp 2        grouped items: copies each query block onto its
@@ -26,7 +28,8 @@
 //                 of warp w owns row 32 (w % 4) + i of its tile.
 // TMEM slot g spans columns [g W, g W + W): S in [0, N) (N = sk rounded up
 // to 32), overwritten by P two 16-bit keys per column in [0, N/2), and the
-// O accumulator in [o_off, o_off + d) once S has been read.
+// O accumulator in [o_off, o_off + d) (64 columns when grouped) once S has
+// been read.
 // The softmax reads S once, 64 columns at a time, with the lazy reference
 // max of the general forward: the first 64 columns set it, and a later pair
 // of chunks whose max exceeds it by more than 8 (log2 units) moves it and

@@ -412,8 +412,7 @@ __device__ __forceinline__ void short_mma_o(uint32_t sbase, uint32_t tiles, uint
     const int kv_steps = a.n_keys / 16;
     for (int n = 0; n < n_items; ++n) {
         const int sl = n % a.nslot, st = n % a.nstage;
-        if (!mbar_wait(bar(BAR_PF + sl), (n / a.nslot) & 1, g, 24)) break;
-        tc_fence_after();
+        // the item's operands, worked out before the wait for its P
         const uint32_t tS = tmem + sl * a.slot_cols;
         int k = 0, ks = 0;
         uint32_t voff;
@@ -425,6 +424,8 @@ __device__ __forceinline__ void short_mma_o(uint32_t sbase, uint32_t tiles, uint
             voff = st * a.stage_bytes + a.q_bytes + a.kv_bytes;
         }
         const uint64_t vd = dv + (voff >> 4);
+        if (!mbar_wait(bar(BAR_PF + sl), (n / a.nslot) & 1, g, 24)) break;
+        tc_fence_after();
         for (int kk = 0; kk < kv_steps; ++kk)
             mma_ts(tS + a.o_off, tS + kk * 8, vd + ((kk * 16 * M::V_ROW) >> 4), idesc_o,
                    kk > 0 ? 1u : 0u);
@@ -554,18 +555,19 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
         if (lane == 0) mbar_arrive(bar(BAR_PF + sl));
 
         // ---------------------------------------------------- epilogue
-        const bool okf = mbar_wait(bar(BAR_OF + sl), k & 1, g, 27);
-        if (!__all_sync(0xffffffffu, okf)) return;
-        tc_fence_after();
-        // O row read out 32 columns at a time (16 at d = 16); the slot goes
-        // back to the MMA issuer as soon as the last piece is in registers,
-        // before that piece is scaled, packed and stored
+        // the row's output address and 1 / l, worked out before the wait for O
         constexpr int OCH = D < 32 ? D : 32;
         const bool row_out = warp_live && grow < a.sq;
         const float inv_l = 1.0f / l;
         const int64_t orow =
             ((static_cast<int64_t>(xb) * a.sq + (row_out ? grow : 0)) * a.h + xh) * D;
         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + orow);
+        const bool okf = mbar_wait(bar(BAR_OF + sl), k & 1, g, 27);
+        if (!__all_sync(0xffffffffu, okf)) return;
+        tc_fence_after();
+        // O row read out 32 columns at a time (16 at d = 16); the slot goes
+        // back to the MMA issuer as soon as the last piece is in registers,
+        // before that piece is scaled, packed and stored
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += OCH) {
             uint32_t ov[OCH];

@@ -795,13 +795,11 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         if (single) pv_done += x.nkv;
 
         // ---------------------------------------------------- epilogue
-        const bool ok = mbar_wait(bar(G::BAR_OF + t), o_cnt & 1, g, 14);
-        ++o_cnt;
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc_fence_after();
         // Read O_t a chunk at a time, normalise, and store: packed to 16 bits
         // into O, or as fp32 into this split's O_i; then hand the accumulator
-        // back to the MMA issuer.
+        // back to the MMA issuer. The epilogue sits between this unit's last
+        // P and the next unit's first softmax on these warps, so what needs
+        // no O (1 / l, the addresses) is worked out before the wait for it.
         // A row that saw no key (causal) has l = 0: O = 0, LSE = -inf.
         const bool empty_row = SPLIT && !(l > 0.0f);
         const float inv_l = empty_row ? 0.0f : 1.0f / l;
@@ -817,6 +815,10 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
               (row_out ? grow : 0)) * a.h + x.head) * D;
         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + orow);
         float *dst_part = a.o_part + orow;
+        const bool ok = mbar_wait(bar(G::BAR_OF + t), o_cnt & 1, g, 14);
+        ++o_cnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
         if (warp_live) {
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += G::OCH) {

@@ -55,7 +55,6 @@ constexpr int SB_PANEL_BYTES = SB_QT * 128;       // 64 keys of 128 query rows, 
 constexpr int SB_PDS_BYTES = 4 * SB_PANEL_BYTES;  // keys 0..255: an M tile reads two whole panels
 constexpr int SB_MAX_N = 160;                     // TMEM: 2 N + 32 (dQ) + 2 x 2 x 32 (dV, dK)
 constexpr int SB_COL_W = 32;                      // columns of a dQ / dV / dK region
-constexpr int SB_CH = SB_MAX_N / 32;              // 16-key chunks per elementwise group
 
 template <int D>
 struct SbGeom {
@@ -393,75 +392,65 @@ __device__ __forceinline__ void sb_elementwise(uint8_t *smem, uint32_t sbase, ui
             const float drow = ld[SBWD_MAX_Q + grow];
             const bool oks = mbar_wait(bar(G::BAR_SF), n_tile & 1, g, 47);
             if (!__all_sync(0xffffffffu, oks)) return;
-            tc_fence_after();
-            // a warp whose 32 rows are all past sq has nothing the MMAs read
-            // (they stop at the tile's last 16-row step holding a query row)
-            const bool live = q4 * 32 < a.sq - qt * SB_QT;
-            // This thread's 16-key chunks j = grp + 2 ci (at most SB_CH of
-            // them): P and dS are made and dS stored into S's columns first,
-            // with the packed P and dS kept in registers; only their copies
-            // into the shared-memory panels wait for the previous tile's dV
-            // and dK MMAs to have read the panels, so that the work runs
-            // beside those MMAs. The next chunk's TMEM loads are in flight
-            // while one is worked on.
-            const uint32_t t_s = tmem + lanes, t_dp = tmem + lanes + p.c_dp;
-            uint32_t hp[SB_CH][8], hd[SB_CH][8];
-            if (live) {
-                uint32_t sv[2][16], pv[2][16];
-                tmem_ld16(t_s + 16 * grp, sv[0]);
-                tmem_ld16(t_dp + 16 * grp, pv[0]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int ci = 0; ci < SB_CH; ++ci) {
-                    const int j = grp + 2 * ci;
-                    if (j < nch16) {
-                        if (j + 2 < nch16) {
-                            tmem_ld16(t_s + 16 * (j + 2), sv[(ci + 1) & 1]);
-                            tmem_ld16(t_dp + 16 * (j + 2), pv[(ci + 1) & 1]);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int k = 16 * j + 2 * e;
-                            float p0 = fast_exp2(__uint_as_float(sv[ci & 1][2 * e]) * c - lse2);
-                            float p1 = fast_exp2(__uint_as_float(sv[ci & 1][2 * e + 1]) * c - lse2);
-                            p0 = k < a.sk ? p0 : 0.f;  // keys past sk (TMA zero fill) take no part
-                            p1 = k + 1 < a.sk ? p1 : 0.f;
-                            hp[ci][e] = sb_pack<BF16>(p0, p1);
-                            hd[ci][e] = sb_pack<BF16>(p0 * (__uint_as_float(pv[ci & 1][2 * e]) - drow),
-                                                      p1 * (__uint_as_float(pv[ci & 1][2 * e + 1]) - drow));
-                        }
-                        // dS of the chunk's 16 keys into its first 8 columns
-                        // (read already, by this thread): the A operand of
-                        // dQ = dS K
-                        tmem_st8(t_s + 16 * j, hd[ci]);
-                        if (j + 2 < nch16) tmem_wait_ld();
-                    }
-                }
-            }
             // the previous tile's dV / dK MMAs have read the P and dS panels
             if (n_tile > 0) {
                 const bool okf = mbar_wait(bar(G::BAR_PFREE), (n_tile - 1) & 1, g, 48);
                 if (!__all_sync(0xffffffffu, okf)) return;
             }
-            if (live) {
+            tc_fence_after();
+            // a warp whose 32 rows are all past sq has nothing the MMAs read
+            // (they stop at the tile's last 16-row step holding a query row)
+            const bool live = q4 * 32 < a.sq - qt * SB_QT;
+            // 16-key chunks j = grp, grp + 2, ...: the next chunk's TMEM loads
+            // are in flight while this one is worked on
+            const uint32_t t_s = tmem + lanes, t_dp = tmem + lanes + p.c_dp;
+            auto work = [&](const uint32_t (&sv)[16], const uint32_t (&pv)[16], int j) {
+                uint32_t pp[8], pd[8];
 #pragma unroll
-                for (int ci = 0; ci < SB_CH; ++ci) {
-                    const int j = grp + 2 * ci;
-                    if (j < nch16) {
-                        // P and dS rows into the panels: keys 16 j .. 16 j + 15
-                        // are 16-byte chunks 2 (j & 3), + 1 of panel j / 4
-                        const int pan = (j >> 2) * SB_PANEL_BYTES;
-                        const int c0 = (j & 3) * 2;
-                        const int o0 = pan + ((c0 ^ sw) << 4), o1 = pan + (((c0 + 1) ^ sw) << 4);
-                        *reinterpret_cast<uint4 *>(prow + o0) =
-                            make_uint4(hp[ci][0], hp[ci][1], hp[ci][2], hp[ci][3]);
-                        *reinterpret_cast<uint4 *>(prow + o1) =
-                            make_uint4(hp[ci][4], hp[ci][5], hp[ci][6], hp[ci][7]);
-                        *reinterpret_cast<uint4 *>(dsrow + o0) =
-                            make_uint4(hd[ci][0], hd[ci][1], hd[ci][2], hd[ci][3]);
-                        *reinterpret_cast<uint4 *>(dsrow + o1) =
-                            make_uint4(hd[ci][4], hd[ci][5], hd[ci][6], hd[ci][7]);
+                for (int e = 0; e < 8; ++e) {
+                    const int k = 16 * j + 2 * e;
+                    float p0 = fast_exp2(__uint_as_float(sv[2 * e]) * c - lse2);
+                    float p1 = fast_exp2(__uint_as_float(sv[2 * e + 1]) * c - lse2);
+                    p0 = k < a.sk ? p0 : 0.f;  // keys past sk (TMA zero fill) take no part
+                    p1 = k + 1 < a.sk ? p1 : 0.f;
+                    pp[e] = sb_pack<BF16>(p0, p1);
+                    pd[e] = sb_pack<BF16>(p0 * (__uint_as_float(pv[2 * e]) - drow),
+                                          p1 * (__uint_as_float(pv[2 * e + 1]) - drow));
+                }
+                // dS of the chunk's 16 keys into its first 8 columns (read
+                // already, by this thread): the A operand of dQ = dS K
+                tmem_st8(t_s + 16 * j, pd);
+                // P and dS rows into the panels: keys 16 j .. 16 j + 15 are
+                // 16-byte chunks 2 (j & 3), + 1 of panel j / 4
+                const int pan = (j >> 2) * SB_PANEL_BYTES;
+                const int c0 = (j & 3) * 2;
+                const int o0 = pan + ((c0 ^ sw) << 4), o1 = pan + (((c0 + 1) ^ sw) << 4);
+                *reinterpret_cast<uint4 *>(prow + o0) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+                *reinterpret_cast<uint4 *>(prow + o1) = make_uint4(pp[4], pp[5], pp[6], pp[7]);
+                *reinterpret_cast<uint4 *>(dsrow + o0) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+                *reinterpret_cast<uint4 *>(dsrow + o1) = make_uint4(pd[4], pd[5], pd[6], pd[7]);
+            };
+            if (live) {
+                uint32_t sa[16], pa[16], sb[16], pb[16];
+                int j = grp;
+                tmem_ld16(t_s + 16 * j, sa);
+                tmem_ld16(t_dp + 16 * j, pa);
+                tmem_wait_ld();
+#pragma unroll 1
+                for (; j < nch16; j += 4) {
+                    if (j + 2 < nch16) {
+                        tmem_ld16(t_s + 16 * (j + 2), sb);
+                        tmem_ld16(t_dp + 16 * (j + 2), pb);
                     }
+                    work(sa, pa, j);
+                    if (j + 2 >= nch16) break;
+                    tmem_wait_ld();
+                    if (j + 4 < nch16) {
+                        tmem_ld16(t_s + 16 * (j + 4), sa);
+                        tmem_ld16(t_dp + 16 * (j + 4), pa);
+                    }
+                    work(sb, pb, j + 2);
+                    tmem_wait_ld();
                 }
             }
             fence_proxy_async_smem();  // the panels, for the tensor core

@@ -240,9 +240,9 @@ __device__ __forceinline__ void short_producer(const CUtensorMap *tq, const CUte
 // Grouped items, run by lane 0 of warp 0: per pair, the group's K and V
 // tiles (n_keys rows of 128 bytes each) into a ring of kv stages; per item,
 // its 32-row query block of the group (128-byte rows) into the stage's
-// staging area. The next pair's K/V is requested after its first query
-// block, once a kv stage has come free (with three kv stages that is the
-// pair before last, long done).
+// staging area. The next pair's K/V is requested right after the current
+// pair's first query block, once a kv stage has come free (with three kv
+// stages, the one the pair before last used: long done).
 // Stage layout (grouped): staging block (32 x 128 bytes), then the
 // block-diagonal query tile (128 x 128 bytes); the kv ring follows the
 // stages: K tile, then V tile, per kv stage.

@@ -60,7 +60,7 @@ def test_query_counts_and_dtypes(gpu, oracle_mod, sq, dtype):
 
 @pytest.mark.parametrize("b,sq,h", [(48, 20, 4), (24, 1, 8), (48, 33, 4), (16, 64, 12), (48, 97, 4),
                                     (24, 150, 8), (48, 200, 4), (24, 256, 8), (32, 150, 6)])
-@pytest.mark.parametrize("sk", [37, 150, 256])
+@pytest.mark.parametrize("sk", [1, 37, 150, 256])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_grouped_heads(gpu, oracle_mod, b, sq, h, sk, dtype):
     """Head dim 16 with the heads in groups of four and more one-head tiles

@@ -134,10 +134,11 @@ struct Unit {
     int sk;  // keys of this unit's sequence (a.sk unless the cache is paged)
 };
 
-// Units are numbered query block first, then split, head and batch. The
-// kernel is compiled with and without key splits (SPLIT): the plain forward
-// keeps the shorter code.
-template <bool SPLIT, bool PAGED>
+// Units are numbered query block first, then split, head and batch. SPLIT
+// picks the kernel's compiled form: 0 the plain forward, 1 the causal forward
+// over all keys of a head, 2 key ranges (split-KV decode, paged caches) with
+// the mask a run-time choice; each keeps only the code it needs.
+template <int SPLIT, bool PAGED>
 __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdArgs &a) {
     Unit x;
     int qb = u % nqb;
@@ -148,9 +149,10 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     // instead keeps a head's units together, but when the grid is a multiple
     // of the query blocks per head it hands each CTA one block index: b4 s512
     // h32 43.7 against 30 us, b16 s1024 h16 157 against 101 us.)
-    if (SPLIT && a.causal) {
-        if (a.longest_first) {
-            const int per = a.splits * a.h * a.b;  // units per query block
+    const bool causal = SPLIT == 1 || (SPLIT == 2 && a.causal);
+    if (causal) {
+        if (SPLIT == 1 || a.longest_first) {
+            const int per = (SPLIT == 2 ? a.splits : 1) * a.h * a.b;  // units per query block
             qb = nqb - 1 - u / per;
             r = u % per;
         } else if (r & 1) {
@@ -161,13 +163,13 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     x.kv0 = 0;
     x.nkv = nkv_all;
     x.sk = a.sk;
-    if constexpr (SPLIT) {
+    if constexpr (SPLIT == 2) {
         x.split = r % a.splits;
         r /= a.splits;
     }
     x.head = r % a.h;
     x.batch = r / a.h;
-    if constexpr (SPLIT) {
+    if constexpr (SPLIT == 2) {
         if constexpr (PAGED) {  // the sequence's own length, on the device
             x.sk = min(max(__ldg(a.seqlens + x.batch), 0), a.sk);
             nkv_all = (x.sk + FWD_BN - 1) / FWD_BN;
@@ -177,8 +179,8 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     }
     x.m0 = qb * (FWD_BM * FWD_QTILES);
     x.n_qt = min(FWD_QTILES, (a.sq - x.m0 + FWD_BM - 1) / FWD_BM);
-    if constexpr (SPLIT) {
-        if (a.causal) {
+    if constexpr (SPLIT != 0) {
+        if (causal) {
             // the unit's last row sees keys up to last + sk - sq: later key
             // tiles are not needed (none at all if that is below 0)
             const int last = min(x.m0 + FWD_BM * FWD_QTILES, a.sq) - 1;
@@ -190,7 +192,7 @@ __device__ __forceinline__ Unit unit_of(int u, int nqb, int nkv_all, const FwdAr
     return x;
 }
 
-template <int D, bool SPLIT, bool PAGED>
+template <int D, int SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtensorMap *tk,
                                              const CUtensorMap *tv, uint32_t sbase, int nqb,
                                              int units, int nkv, const FwdArgs &a,
@@ -252,7 +254,7 @@ __device__ __forceinline__ void fwd_producer(const CUtensorMap *tq, const CUtens
 // wholly past the sequence's end is addressed past the last pool page, so
 // TMA fills it with zeros; rows past the end inside the last box hold stale
 // data (masked for K, zeroed for V before the P V MMA).
-template <int D, bool SPLIT, bool PAGED>
+template <int D, int SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_producer_paged(const CUtensorMap *tq, const CUtensorMap *tk,
                                                    const CUtensorMap *tv, uint32_t sbase, int nqb,
                                                    int units, int nkv, const FwdArgs &a,
@@ -343,7 +345,7 @@ __device__ __forceinline__ bool unit_needs_v_fix(const Unit &x) {
     return PAGED && x.nkv > 0 && (x.kv0 + x.nkv) * FWD_BN > x.sk;
 }
 
-template <int D, bool SPLIT, bool PAGED>
+template <int D, int SPLIT, bool PAGED>
 __device__ __forceinline__ void fwd_fix_v(uint32_t sbase, int nqb, int units, int nkv,
                                           const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
@@ -381,7 +383,7 @@ __device__ __forceinline__ void fwd_fix_v(uint32_t sbase, int nqb, int units, in
     }
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
+template <int D, bool BF16, int SPLIT, bool PAGED, bool ONE>
 __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, int units,
                                         int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
@@ -580,7 +582,7 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
     mbar_wait(bar(G::BAR_DONE), 0, drain, 12);
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
+template <int D, bool BF16, int SPLIT, bool PAGED, bool ONE>
 __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t, int q4, int nqb,
                                             int units, int nkv, const FwdArgs &a,
                                             const WaitGuard &g) {
@@ -633,8 +635,8 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 int valid = x.sk - (x.kv0 + j) * G::BN;
                 int vmax = valid;
                 bool ragged = valid < G::BN;
-                if constexpr (SPLIT) {
-                    if (a.causal) {
+                if constexpr (SPLIT != 0) {
+                    if (SPLIT == 1 || a.causal) {
                         valid = min(valid, grow + x.sk - a.sq + 1 - (x.kv0 + j) * G::BN);
                         vmax = __reduce_max_sync(0xffffffffu, valid);
                         ragged = __any_sync(0xffffffffu, valid < G::BN);
@@ -804,9 +806,9 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
         const bool empty_row = SPLIT && !(l > 0.0f);
         const float inv_l = empty_row ? 0.0f : 1.0f / l;
         const bool row_out = warp_live && grow < a.sq;
-        // fp32 partials only with more than one split (the SPLIT instantiation
-        // also runs causal calls with one split, which write O and LSE)
-        const bool part = SPLIT && a.splits > 1;
+        // fp32 partials only with more than one split (key ranges with one
+        // split, paged or several-row decode calls, write O and LSE)
+        const bool part = SPLIT == 2 && a.splits > 1;
         // Rows start at multiples of 2d bytes (>= 32); only the base of O may
         // be merely 16-byte aligned. The fp32 partials are allocated here.
         const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
@@ -873,7 +875,7 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     }
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
+template <int D, bool BF16, int SPLIT, bool PAGED, bool ONE>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -948,7 +950,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, G::TMEM_COLS);
 }
 
-template <int D, bool BF16, bool SPLIT, bool PAGED, bool ONE>
+template <int D, bool BF16, int SPLIT, bool PAGED, bool ONE>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
     using G = FwdGeom<D>;
@@ -984,7 +986,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 // 32.8 -> 33.9 us), so the two-tile kernel keeps those. The two paths are
 // separate kernels: compiled into one, the two-tile calls lost about 6 us
 // per launch (b4 s512 h32: 26.6 -> 32.8 us) though they never ran the other.
-template <int D, bool BF16, bool SPLIT, bool PAGED>
+template <int D, bool BF16, int SPLIT, bool PAGED>
 cudaError_t launch_fwd_o(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
     return a.sq <= FWD_BM && a.sk > FWD_BN
@@ -995,11 +997,15 @@ cudaError_t launch_fwd_o(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 template <int D, bool BF16>
 cudaError_t launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdArgs &a, cudaStream_t stream) {
-    // three instantiations: the plain forward, key ranges / causal, and key
-    // ranges over a paged cache; each keeps only the code it needs
-    if (a.block_table) return launch_fwd_o<D, BF16, true, true>(tq, tk, tv, a, stream);
-    return (a.splits > 1 || a.causal) ? launch_fwd_o<D, BF16, true, false>(tq, tk, tv, a, stream)
-                                      : launch_fwd_o<D, BF16, false, false>(tq, tk, tv, a, stream);
+    // four instantiations: the plain forward, the causal forward (one key
+    // range, no partials), key ranges (with or without the mask), and key
+    // ranges over a paged cache; each keeps only the code it needs (the
+    // causal forward on the key-range kernel: b8 s256 h32 d128 26.6 against
+    // 24.6 us, b2 s1024 h48 47.4 against 45.0)
+    if (a.block_table) return launch_fwd_o<D, BF16, 2, true>(tq, tk, tv, a, stream);
+    if (a.splits > 1) return launch_fwd_o<D, BF16, 2, false>(tq, tk, tv, a, stream);
+    return a.causal ? launch_fwd_o<D, BF16, 1, false>(tq, tk, tv, a, stream)
+                    : launch_fwd_o<D, BF16, 0, false>(tq, tk, tv, a, stream);
 }
 
 }  // namespace

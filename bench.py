@@ -117,10 +117,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each captured kernel is compiled from
+KERNEL_SOURCES = {
+    "fwd_mid": ("exact_attention_65_gb300/csrc/fwd.cu", "exact_attention_65_gb300/csrc/ptx.cuh",
+                "exact_attention_65_gb300/csrc/internal.h"),
+    "decode_b1": ("exact_attention_65_gb300/csrc/decode.cu", "exact_attention_65_gb300/csrc/ptx.cuh",
+                  "exact_attention_65_gb300/csrc/internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in ("exact_attention_65_gb300/csrc/fwd.cu", "exact_attention_65_gb300/csrc/decode.cu",
-                "exact_attention_65_gb300/csrc/ptx.cuh", "exact_attention_65_gb300/csrc/internal.h"):
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -128,17 +136,17 @@ def kernel_source_hash() -> str:
 
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; otherwise None."""
+    on the kernel's current sources; otherwise None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("source_sha256") != kernel_source_hash():
-        return None
     e = d.get("kernels", {}).get(kernel)
-    return None if e is None else e.get("dram_bytes_per_launch")
+    if e is None or e.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------------ clocks

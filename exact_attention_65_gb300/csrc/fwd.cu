@@ -49,6 +49,9 @@
 namespace exattn {
 namespace {
 
+// Bit 13 of a kind::f16 instruction descriptor: negate the A operand.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 template <int D>
 struct FwdGeom {
     static constexpr int BM = FWD_BM;
@@ -388,7 +391,10 @@ __device__ __forceinline__ void fwd_mma(uint32_t sbase, uint32_t tmem, int nqb, 
                                         int nkv, const FwdArgs &a, const WaitGuard &g) {
     using G = FwdGeom<D>;
     auto bar = [&](int i) { return sbase + G::OFF_BAR + 8u * i; };
-    constexpr uint32_t idesc_s = mma_idesc_f16(G::BM, G::BN, BF16, false, false);
+    // with a negative scale the S MMAs negate Q, so that the softmax always
+    // works with a scale >= 0 (the products are the same, negation is exact)
+    const uint32_t idesc_s = mma_idesc_f16(G::BM, G::BN, BF16, false, false) |
+                             (a.scale_log2 < 0.f ? kIdescNegateA : 0u);
     constexpr uint32_t idesc_o = mma_idesc_f16(G::BM, D, BF16, false, true);
     // This one thread issues every MMA of the CTA and is on the critical path,
     // so descriptors are built once here: the start-address field is the low
@@ -592,8 +598,10 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
     const int row = q4 * 32 + lane;
     const uint32_t tS0 = tmem + t * G::TMEM_TILE_STRIDE + (static_cast<uint32_t>(q4 * 32) << 16);
     const uint32_t tO = tS0 + G::TMEM_O_OFF;
-    const float c = a.scale_log2;
-    const bool c_pos = c >= 0.f;
+    // S arrives as sign(scale) * QK^T (the S MMAs negate Q for a negative
+    // scale): with c = |scale| log2 e, the row max of the raw scores is the
+    // max of the scaled ones
+    const float c = fabsf(a.scale_log2);
     int s_cnt = 0, o_cnt = 0;
     // one-tile units (tile 0's warpgroup only): S phases of odd key tiles,
     // and P V products issued so far
@@ -644,10 +652,10 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                 }
                 uint32_t sr[G::BN];
                 const float *s = reinterpret_cast<const float *>(sr);
-                // row max of the scaled scores (min of the raw ones if scale < 0)
+                // row max of the scores
                 float mx[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) mx[i] = c_pos ? -INFINITY : INFINITY;
+                for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
                 if (!ragged) {
                     // the max of the first 64 scores runs while the rest load
                     tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -658,15 +666,9 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1) tmem_wait_ld();
-                        if (c_pos) {
 #pragma unroll
-                            for (int i = part * G::BN / 4; i < (part + 1) * G::BN / 4; ++i)
-                                mx[i & 3] = max3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
-                        } else {
-#pragma unroll
-                            for (int i = part * G::BN / 4; i < (part + 1) * G::BN / 4; ++i)
-                                mx[i & 3] = min3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
-                        }
+                        for (int i = part * G::BN / 4; i < (part + 1) * G::BN / 4; ++i)
+                            mx[i & 3] = max3f(mx[i & 3], s[2 * i], s[2 * i + 1]);
                     }
                 } else {
 #pragma unroll
@@ -681,14 +683,12 @@ __device__ __forceinline__ void fwd_softmax(uint32_t sbase, uint32_t tmem, int t
                         if (c0 < vmax) {
 #pragma unroll
                             for (int i = c0; i < c0 + 32; ++i) {
-                                if (i < valid)
-                                    mx[i & 3] = c_pos ? fmaxf(mx[i & 3], s[i]) : fminf(mx[i & 3], s[i]);
+                                if (i < valid) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
                             }
                         }
                     }
                 }
-                const float mraw = c_pos ? fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3])
-                                         : fminf(min3f(mx[0], mx[1], mx[2]), mx[3]);
+                const float mraw = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
                 const float m_tile = mraw * c;
 
                 const bool need = m_tile > m_ref + 8.0f;

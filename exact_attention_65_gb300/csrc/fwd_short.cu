@@ -66,6 +66,9 @@
 namespace exattn {
 namespace {
 
+// Bit 13 of a kind::f16 instruction descriptor: negate the A operand.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 constexpr int SH_WG = SHORT_MAX_SLOTS;          // most softmax warpgroups
 constexpr int SH_BAR_BYTES = 1024;             // barriers and flags, before the tiles
 
@@ -136,17 +139,16 @@ __device__ __forceinline__ GroupItem group_item(int n, int nblk, int hg) {
     return x;
 }
 
-// Folds one 32-column chunk of raw scores into four running maxima (minima
-// when scale < 0). MASK: only the first `valid` columns are keys.
-template <bool MASK, bool POS>
-__device__ __forceinline__ void chunk_extreme(const uint32_t (&r)[32], int valid, float (&mx)[4]) {
+// Folds one 32-column chunk of scores into four running maxima. MASK: only
+// the first `valid` columns are keys.
+template <bool MASK>
+__device__ __forceinline__ void chunk_max(const uint32_t (&r)[32], int valid, float (&mx)[4]) {
     const float *s = reinterpret_cast<const float *>(r);
-    const float pad = POS ? -INFINITY : INFINITY;
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        const float x0 = (!MASK || 2 * e < valid) ? s[2 * e] : pad;
-        const float x1 = (!MASK || 2 * e + 1 < valid) ? s[2 * e + 1] : pad;
-        mx[e & 3] = POS ? max3f(mx[e & 3], x0, x1) : min3f(mx[e & 3], x0, x1);
+        const float x0 = (!MASK || 2 * e < valid) ? s[2 * e] : -INFINITY;
+        const float x1 = (!MASK || 2 * e + 1 < valid) ? s[2 * e + 1] : -INFINITY;
+        mx[e & 3] = max3f(mx[e & 3], x0, x1);
     }
 }
 
@@ -355,7 +357,10 @@ __device__ __forceinline__ void short_mma_s(uint32_t sbase, uint32_t tiles, uint
                                             const WaitGuard &g) {
     using M = MmaGeom<D, GRP>;
     auto bar = [&](int i) { return sbase + 8u * i; };
-    const uint32_t idesc_s = mma_idesc_f16(SHORT_BM, a.n_keys, BF16, false, false);
+    // with a negative scale the S MMAs negate Q, so that the softmax always
+    // works with a scale >= 0 (the products are the same, negation is exact)
+    const uint32_t idesc_s = mma_idesc_f16(SHORT_BM, a.n_keys, BF16, false, false) |
+                             (a.scale_log2 < 0.f ? kIdescNegateA : 0u);
     const uint64_t dk = smem_desc(tiles, 16, M::SBO, M::LAYOUT);  // Q and K, K-major
     const uint32_t kv_base = a.nstage * a.stage_bytes;  // grouped: the kv ring, after the stages
     for (int n = 0; n < n_items; ++n) {
@@ -448,8 +453,9 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t tS = tmem + sl * a.slot_cols + (static_cast<uint32_t>(q4 * 32) << 16);
     const uint32_t tO = tS + a.o_off;
-    const float c = a.scale_log2;
-    const bool c_pos = c >= 0.f;
+    // S arrives as sign(scale) * QK^T: with c = |scale| log2 e, the row max
+    // of the raw scores is the max of the scaled ones
+    const float c = fabsf(a.scale_log2);
     const int nch = a.n_keys / 32;
     // keys of the last 32-column chunk that exist (1..32)
     const int last_valid = a.sk - 32 * (nch - 1);
@@ -484,8 +490,7 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
         float m_ref = -INFINITY, l = 1.f;
         if (warp_live) {
             // One pass over S, two 32-column chunks per TMEM round trip: the
-            // pair's max (of the raw scores, their min if scale < 0) moves the
-            // reference max only past the lazy threshold; then its P is
+            // pair's max moves the reference max only past the lazy threshold; then its P is
             // stored into the pair's first 32 columns, whose scores have been
             // read. Only the last chunk can be ragged.
             const uint64_t c2 = f2_make(c, c);
@@ -499,23 +504,17 @@ __device__ __forceinline__ void short_softmax(uint32_t sbase, uint32_t tmem, int
                     tmem_wait_ld();
                     float mx[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) mx[q] = c_pos ? -INFINITY : INFINITY;
+                    for (int q = 0; q < 4; ++q) mx[q] = -INFINITY;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int cc = ch + h2;
                         if (cc < nch) {
                             const bool ragged = cc == nch - 1 && last_valid < 32;
-                            if (c_pos) {
-                                if (ragged) chunk_extreme<true, true>(r[h2], last_valid, mx);
-                                else chunk_extreme<false, true>(r[h2], 32, mx);
-                            } else {
-                                if (ragged) chunk_extreme<true, false>(r[h2], last_valid, mx);
-                                else chunk_extreme<false, false>(r[h2], 32, mx);
-                            }
+                            if (ragged) chunk_max<true>(r[h2], last_valid, mx);
+                            else chunk_max<false>(r[h2], 32, mx);
                         }
                     }
-                    const float mraw = c_pos ? fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3])
-                                             : fminf(min3f(mx[0], mx[1], mx[2]), mx[3]);
+                    const float mraw = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
                     const float m_pair = mraw * c;  // log2 units
                     const bool need = m_pair > m_ref + 8.0f;
                     // 0 on the first pair (nothing stored yet), 1 where kept;

@@ -498,7 +498,7 @@ int dec_num_splits(int b, int sq, int sk, int h, int d, int num_sms) {
 
 extern "C" {
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 101; }
 
 const char *attn_status_string(attn_status_t s) {
     switch (s) {

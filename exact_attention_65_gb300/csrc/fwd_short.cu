@@ -820,3 +820,15 @@ cudaError_t launch_fwd_short(int d, bool bf16, const CUtensorMap &tq, const CUte
 }
 
 }  // namespace exattn
+
+extern "C" int attn_debug_short_plan(int sq, int sk, int h, int d, int grouped_ok, int *out) {
+    exattn::ShortArgs a{};
+    if (out == nullptr || !exattn::short_plan(sq, sk, h, d, grouped_ok != 0, &a)) return 0;
+    // grouped: the query stages, then the K/V ring; plain: the stages alone
+    const int used = a.nstage * a.stage_bytes + (a.grouped ? a.nkv_stage * a.kv_stage_bytes : 0);
+    const int v[12] = {a.n_keys,  a.o_off, a.slot_cols, a.nslot,     a.kv_bytes, a.stage_bytes,
+                       a.nstage,  a.grouped, a.nblk,    a.nkv_stage, used,
+                       exattn::SHORT_SMEM_BYTES - 1024 - exattn::SH_BAR_BYTES};
+    for (int i = 0; i < 12; ++i) out[i] = v[i];
+    return 1;
+}

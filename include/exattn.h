@@ -337,7 +337,28 @@ void attn_release_workspace(void);
 #define ATTN_DEBUG_GENERAL_BWD 4u
 void attn_debug_set_flags(unsigned int flags);
 
-/* Library ABI version (major * 100 + minor). */
+/*
+ * Test hook, host-side only (launches nothing, needs no GPU): the plan the
+ * short forward kernel (all keys of a head in one tile) would run a forward
+ * of sq query rows, sk keys, h heads and head dim d with. grouped_ok != 0
+ * allows heads in groups of four (attn_fwd allows it when the one-head tiles
+ * outnumber the SMs). Returns 1 and writes 12 ints to out (caller-owned):
+ *   out[0] key columns N of S (sk rounded up to 32)
+ *   out[1] TMEM column of the O accumulator within a slot
+ *   out[2] TMEM columns of one slot       out[3] slots (items in flight)
+ *   out[4] bytes of one K or V tile       out[5] bytes of one stage
+ *   out[6] stages                         out[7] 1 if heads are grouped
+ *   out[8] 32-row query blocks per head (grouped; else 0)
+ *   out[9] K/V stages (grouped; else 0)
+ *   out[10] shared-memory bytes the tiles take
+ *   out[11] shared-memory bytes available to them
+ * Returns 0 and leaves out untouched when the short kernel does not take
+ * the shape (sq, sk or h below 1, sk > 256, d not 16, 32 or 64) or out is
+ * NULL.
+ */
+int attn_debug_short_plan(int sq, int sk, int h, int d, int grouped_ok, int *out);
+
+/* Library ABI version (major * 100 + minor): 101. */
 int attn_version(void);
 
 #ifdef __cplusplus

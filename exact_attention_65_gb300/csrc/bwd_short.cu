@@ -55,6 +55,7 @@ constexpr int SB_PANEL_BYTES = SB_QT * 128;       // 64 keys of 128 query rows, 
 constexpr int SB_PDS_BYTES = 4 * SB_PANEL_BYTES;  // keys 0..255: an M tile reads two whole panels
 constexpr int SB_MAX_N = 160;                     // TMEM: 2 N + 32 (dQ) + 2 x 2 x 32 (dV, dK)
 constexpr int SB_COL_W = 32;                      // columns of a dQ / dV / dK region
+static_assert(2 * SB_MAX_N + SB_COL_W + 2 * 2 * SB_COL_W <= 512, "TMEM columns of the widest item");
 
 template <int D>
 struct SbGeom {
